@@ -1,0 +1,278 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+None of these compares the oracle with itself: each expected value comes from
+a fixture written by hand from the code table, a second formulation of the
+table, a closed form, a balanced-ternary identity, or a library matmul.
+"""
+import numpy as np
+import pytest
+
+from conftest import read_golden
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+def table_from_golden():
+    return {int(bits, 2): int(v) for bits, v in read_golden("code_table.txt")}
+
+
+def second_formulation(packed):
+    """The table as the 7B write-up states it in §2.2: sign = (code==1) - (code==2),
+    fields read at shifts 0,2,4,6 (low bits first)."""
+    b = packed.astype(np.int16)[..., None]
+    codes = (b >> np.array([0, 2, 4, 6])) & 3
+    t = (codes == 1).astype(np.int8) - (codes == 2).astype(np.int8)
+    return t.reshape(packed.shape[0], packed.shape[1] * 4)
+
+
+def test_code_table(oracle_mod):
+    table = table_from_golden()
+    assert sorted(table) == [0, 1, 2, 3]
+    for code, v in table.items():
+        assert oracle_mod.trit(code) == v
+
+
+def test_byte_0x1a_reads_low_bits_first(oracle_mod):
+    (row,) = read_golden("byte_0x1a.txt")
+    byte = int(row[0], 16)
+    want = [int(v) for v in row[1:]]
+    t, reserved = oracle_mod.unpack(np.array([[byte]], dtype=np.uint8))
+    assert t[0].tolist() == want
+    assert reserved == 0
+
+
+def test_all_256_bytes_against_second_formulation(oracle_mod):
+    packed = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    t, reserved = oracle_mod.unpack(packed)
+    assert np.array_equal(t, second_formulation(packed))
+    # every byte with a field equal to 11: count fields by brute force
+    want_reserved = sum(((b >> s) & 3) == 3 for b in range(256) for s in (0, 2, 4, 6))
+    assert reserved == want_reserved == 256 * 4 // 4
+
+
+def test_all_256_bytes_against_golden_table(oracle_mod):
+    table = table_from_golden()
+    packed = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    t, _ = oracle_mod.unpack(packed)
+    for b in range(256):
+        want = [table[(b >> (2 * j)) & 3] for j in range(4)]
+        assert t[b].tolist() == want, hex(b)
+
+
+def test_unpack_wider_row_field_positions(oracle_mod):
+    # one non-zero field per row, at every position of a 3-byte row: catches a
+    # wrong byte index or field order
+    K = 12
+    for k in range(K):
+        for code, v in ((1, 1), (2, -1)):
+            packed = np.zeros((1, K // 4), dtype=np.uint8)
+            packed[0, k // 4] = code << (2 * (k % 4))
+            t, _ = oracle_mod.unpack(packed)
+            want = np.zeros(K, dtype=np.int8)
+            want[k] = v
+            assert np.array_equal(t[0], want)
+
+
+def test_pack_roundtrip_random(oracle_mod):
+    rng = np.random.default_rng(1)
+    t = rng.integers(-1, 2, size=(37, 64), dtype=np.int8)
+    packed, invalid = oracle_mod.pack(t)
+    assert invalid == 0
+    back, reserved = oracle_mod.unpack(packed)
+    assert reserved == 0
+    assert np.array_equal(back, t)
+    # and the packed bytes agree with the second formulation
+    assert np.array_equal(second_formulation(packed), t)
+
+
+def test_pack_of_unpack_canonicalises_reserved(oracle_mod):
+    packed = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    t, _ = oracle_mod.unpack(packed)
+    again, invalid = oracle_mod.pack(t)
+    assert invalid == 0
+    # 11 fields become 00; every other field is unchanged
+    canon = packed.copy()
+    for b in range(256):
+        c = b
+        for j in range(4):
+            if ((b >> (2 * j)) & 3) == 3:
+                c &= ~(3 << (2 * j)) & 0xFF
+        canon[b, 0] = c
+    assert np.array_equal(again, canon)
+
+
+def test_pack_counts_invalid(oracle_mod):
+    t = np.array([[0, 1, -1, 2, 5, -3, 0, 0]], dtype=np.int8)
+    packed, invalid = oracle_mod.pack(t)
+    assert invalid == 3
+    assert packed[0].tolist() == [0b00_10_01_00 | 0, 0]  # invalid entries written as 00
+
+
+def test_hand_example(oracle_mod):
+    rows = read_golden("linear_hand_example.txt")
+    packed = np.array([[int(v, 16) for v in r[1:]] for r in rows if r[0] == "packed"],
+                      dtype=np.uint8)
+    x = np.array([[float(v) for v in r[1:]] for r in rows if r[0] == "x"])
+    kv = {r[0]: r[1:] for r in rows if r[0] not in ("packed", "x")}
+    s_ch = np.array([float(v) for v in kv["channel_scale"]])
+    y_ch = np.array([float(v) for v in kv["channel_y"]]).reshape(2, 2)
+    G = int(kv["group_size"][0])
+    s_g = np.array([float(v) for v in kv["group_scale"]]).reshape(2, -1)
+    y_g = np.array([float(v) for v in kv["group_y"]]).reshape(2, 2)
+    assert np.array_equal(oracle_mod.linear_f64(x, packed, s_ch, 0), y_ch)
+    assert np.array_equal(oracle_mod.linear_f64(x, packed, s_g, G), y_g)
+
+
+def test_brute_force_every_byte_balanced_ternary(oracle_mod):
+    """Row n = byte n, K=4, x = (1,3,9,27), s = 1: y[n] is the balanced-ternary
+    number whose digits are the row's four values, so it identifies them."""
+    packed = np.arange(256, dtype=np.uint8).reshape(256, 1)
+    x = np.array([[1.0, 3.0, 9.0, 27.0]])
+    y = oracle_mod.linear_f64(x, packed, np.ones(256), 0)[0]
+    table = table_from_golden()
+    for b in range(256):
+        digits = [table[(b >> (2 * j)) & 3] for j in range(4)]
+        assert y[b] == sum(d * 3 ** j for j, d in enumerate(digits))
+    # distinct digit vectors give distinct values: decode back
+    for b in range(256):
+        v, got = int(y[b]), []
+        for _ in range(4):
+            r = ((v + 1) % 3) - 1
+            got.append(r)
+            v = (v - r) // 3
+        assert got == [table[(b >> (2 * j)) & 3] for j in range(4)]
+
+
+@pytest.mark.parametrize("group_size", [0, 128])
+def test_closed_forms(oracle_mod, group_size):
+    rng = np.random.default_rng(7)
+    M, K = 3, 256
+    x = rng.standard_normal((M, K))
+    groups = K // 128
+    rows = {
+        "plus": 0x55,   # every field 01
+        "minus": 0xAA,  # every field 10
+        "zero": 0x00,
+        "reserved": 0xFF,
+    }
+    packed = np.stack([np.full(K // 4, v, dtype=np.uint8) for v in rows.values()])
+    N = packed.shape[0]
+    if group_size == 0:
+        s = np.array([0.5, 0.25, 3.0, 7.0])
+        y = oracle_mod.linear_f64(x, packed, s, 0)
+        np.testing.assert_allclose(y[:, 0], 0.5 * x.sum(1), rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(y[:, 1], -0.25 * x.sum(1), rtol=1e-13, atol=1e-13)
+    else:
+        s = np.array([[0.5, 2.0], [0.25, 4.0], [3.0, 1.0], [7.0, 1.0]])
+        y = oracle_mod.linear_f64(x, packed, s, 128)
+        want0 = 0.5 * x[:, :128].sum(1) + 2.0 * x[:, 128:].sum(1)
+        want1 = -(0.25 * x[:, :128].sum(1) + 4.0 * x[:, 128:].sum(1))
+        np.testing.assert_allclose(y[:, 0], want0, rtol=1e-13, atol=1e-13)
+        np.testing.assert_allclose(y[:, 1], want1, rtol=1e-13, atol=1e-13)
+    assert np.all(y[:, 2] == 0.0) and np.all(y[:, 3] == 0.0)
+    assert y.shape == (M, N)
+
+
+def test_one_hot_weight_picks_one_input(oracle_mod):
+    rng = np.random.default_rng(3)
+    M, K = 2, 512
+    x = rng.standard_normal((M, K))
+    for k in (0, 1, 2, 3, 127, 128, 300, 511):
+        for code, sign in ((1, 1.0), (2, -1.0)):
+            packed = np.zeros((1, K // 4), dtype=np.uint8)
+            packed[0, k // 4] = code << (2 * (k % 4))
+            s = np.full((1, K // 128), 0.0)
+            s[0, k // 128] = 0.75
+            y = oracle_mod.linear_f64(x, packed, s, 128)
+            assert np.array_equal(y[:, 0], sign * 0.75 * x[:, k])
+            y = oracle_mod.linear_f64(x, packed, np.array([1.5]), 0)
+            assert np.array_equal(y[:, 0], sign * 1.5 * x[:, k])
+
+
+def test_group_isolation(oracle_mod):
+    rng = np.random.default_rng(5)
+    M, K, N = 2, 512, 3
+    x = rng.standard_normal((M, K))
+    packed = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    t = second_formulation(packed)
+    for g in range(K // 128):
+        s = np.zeros((N, K // 128))
+        s[:, g] = 1.0
+        y = oracle_mod.linear_f64(x, packed, s, 128)
+        want = x[:, g * 128:(g + 1) * 128] @ t[:, g * 128:(g + 1) * 128].T.astype(np.float64)
+        np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("group_size", [0, 128, 64])
+def test_matches_library_matmul(oracle_mod, group_size):
+    """The oracle equals numpy's fp64 matmul of x and the dequantised weight
+    (t * s broadcast per row / per group) to rounding."""
+    rng = np.random.default_rng(11)
+    M, N, K = 5, 33, 512
+    x = rng.standard_normal((M, K))
+    packed = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    t = second_formulation(packed).astype(np.float64)
+    if group_size == 0:
+        s = rng.uniform(0.01, 0.05, size=N)
+        w = t * s[:, None]
+    else:
+        s = rng.uniform(0.01, 0.05, size=(N, K // group_size))
+        w = t * np.repeat(s, group_size, axis=1)
+    y = oracle_mod.linear_f64(x, packed, s, group_size)
+    ref = np.matmul(x, w.T)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_linearity_and_row_independence(oracle_mod):
+    rng = np.random.default_rng(13)
+    M, N, K = 4, 9, 256
+    x1 = rng.standard_normal((M, K))
+    x2 = rng.standard_normal((M, K))
+    packed = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    s = rng.uniform(0.01, 0.05, size=(N, 2))
+    y1 = oracle_mod.linear_f64(x1, packed, s, 128)
+    y2 = oracle_mod.linear_f64(x2, packed, s, 128)
+    y12 = oracle_mod.linear_f64(2.0 * x1 - x2, packed, s, 128)
+    np.testing.assert_allclose(y12, 2.0 * y1 - y2, rtol=1e-12, atol=1e-12)
+    ys = oracle_mod.linear_f64(x1, packed, 4.0 * s, 128)
+    assert np.array_equal(ys, 4.0 * y1)
+    # a token row of the output depends only on that token row of x
+    y_row = oracle_mod.linear_f64(x1[2:3], packed, s, 128)
+    assert np.array_equal(y_row[0], y1[2])
+
+
+def test_fused_rows_equal_shards(oracle_mod):
+    """A fused layer (rows of several shards stacked, scale rows stacked at the
+    same offsets) gives each shard's standalone result in its columns."""
+    rng = np.random.default_rng(17)
+    M, K = 3, 256
+    shards = [5, 2, 2]
+    x = rng.standard_normal((M, K))
+    packs = [rng.integers(0, 256, size=(n, K // 4), dtype=np.uint8) for n in shards]
+    scales = [rng.uniform(0.01, 0.05, size=(n, 2)) for n in shards]
+    fused = oracle_mod.linear_f64(x, np.concatenate(packs), np.concatenate(scales), 128)
+    off = 0
+    for p, s in zip(packs, scales):
+        part = oracle_mod.linear_f64(x, p, s, 128)
+        assert np.array_equal(fused[:, off:off + p.shape[0]], part)
+        off += p.shape[0]
+
+
+def test_threads_do_not_change_results(oracle_mod):
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((3, 384))
+    packed = rng.integers(0, 256, size=(50, 96), dtype=np.uint8)
+    s = rng.uniform(0.01, 0.05, size=(50, 3))
+    a = oracle_mod.linear_f64(x, packed, s, 128, nthreads=1)
+    b = oracle_mod.linear_f64(x, packed, s, 128, nthreads=7)
+    assert np.array_equal(a, b)
+
+
+def test_bit_conversions_exact(oracle_mod):
+    import torch
+    v = torch.randn(1000, generator=torch.Generator().manual_seed(0))
+    for dt, name in ((torch.float16, "f16"), (torch.bfloat16, "bf16")):
+        t = v.to(dt)
+        bits = t.view(torch.int16).numpy().view(np.uint16)
+        got = oracle_mod.bits_to_f64(bits, name)
+        assert np.array_equal(got, t.to(torch.float64).numpy())
