@@ -1,0 +1,427 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary-weight linear layer on GB300.
+
+Default workload: the 7B-shaped decode set (N,K) in {(4096,4096) q/k/v/o,
+(11008,4096) gate/up, (4096,11008) down}, bf16 x, per-channel fp16 scales,
+M in {1,4,8,16}, run as decode steps through a 32-layer stack whose every
+layer has its own weights (1.62 GB of packed weights per M, far above the
+129 MB L2, so no flush is needed).  One bench step = one decode pass at each
+M (4 x 224 = 896 ternary_linear calls), captured once as a CUDA graph and
+replayed.
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
+(the layer shards across GPUs only as independent replicas here; no
+collective is on the data path): value = sum of ranks' work / max rank time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg2]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ternary_weight_linear_02_gb300 import synth  # noqa: E402
+from ternary_weight_linear_02_gb300.workloads import CONFIGS, algorithmic_bytes, flops, packed_bytes  # noqa: E402
+
+METRIC = "packed-weight HBM GB/s and % of roofline per ternary_linear; µs/decode-step"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples, kept only inside [t0, t1]."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.t0 = self.t1 = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = [s for (t, s) in self.samples if self.t0 is not None and self.t0 <= t <= self.t1 + 0.15]
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [c.strip() for c in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workload
+class Stack:
+    """Device-resident inputs of one config: per model layer, per projection,
+    packed weights and scales; per M, x and out buffers for every call."""
+
+    def __init__(self, cfg, Ms, dev):
+        self.cfg, self.Ms, self.dev = cfg, Ms, dev
+        self.w = []  # [depth][proj] -> (packed, scale)
+        for d in range(cfg.depth):
+            row = []
+            for l in cfg.layers:
+                packed = synth.packed_codes(l.N, l.K, synth.seed_for(cfg.key, d, l.name, "w"), dev,
+                                            cfg.p_reserved)
+                groups = 0 if cfg.group_size == 0 else l.K // cfg.group_size
+                scale = synth.scales(l.N, groups, cfg.s_lo, cfg.s_hi,
+                                     synth.seed_for(cfg.key, d, l.name, "s"), dev)
+                row.append((packed, scale))
+            self.w.append(row)
+        self.x, self.out = {}, {}
+        for M in Ms:
+            xs, outs = [], []
+            for d in range(cfg.depth):
+                xr, orow = [], []
+                for l in cfg.layers:
+                    xr.append(synth.activations(M, l.K, cfg.x_dtype,
+                                                synth.seed_for(cfg.key, d, l.name, "x", M), dev))
+                    orow.append(torch.empty((M, l.N), dtype=cfg.x_dtype, device=dev))
+                xs.append(xr)
+                outs.append(orow)
+            self.x[M], self.out[M] = xs, outs
+
+    def calls_per_step(self):
+        return len(self.Ms) * self.cfg.depth * len(self.cfg.layers)
+
+    def run_step(self, tl):
+        cfg = self.cfg
+        for M in self.Ms:
+            for d in range(cfg.depth):
+                for j, l in enumerate(cfg.layers):
+                    packed, scale = self.w[d][j]
+                    tl.linear(self.x[M][d][j], packed, scale, cfg.group_size,
+                              out=self.out[M][d][j])
+
+
+def capture(fn, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def time_graph(g, stream, steps, warmup, barrier):
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    barrier()
+    return e0.elapsed_time(e1), t0, t1
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(cfg, Ms, budget_s: float, threads: int):
+    """Time the CPU oracle on a bounded sample of the workload: for each
+    projection shape, a slice of output rows at every M.  Returns
+    (packed GB/s of the sample, description)."""
+    import oracle
+    oracle.build()
+    done_bytes, spent = 0, 0.0
+    shapes = {}
+    for l in cfg.layers:
+        shapes.setdefault((l.N, l.K), l)
+    per_shape = budget_s / max(1, len(shapes) * len(Ms))
+    rows_used = {}
+    for (N, K), l in shapes.items():
+        for M in Ms:
+            x = synth.activations(M, K, cfg.x_dtype, synth.seed_for("cpu", K, M), "cpu")
+            xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
+            name = "f16" if cfg.x_dtype == torch.float16 else "bf16"
+            # calibrate on a small slice, then size the slice to the budget
+            rows = max(threads, 8)
+            while True:
+                p = synth.packed_codes(rows, K, synth.seed_for("cpu", N, K, rows), "cpu").numpy()
+                groups = 0 if cfg.group_size == 0 else K // cfg.group_size
+                s = synth.scales(rows, groups, cfg.s_lo, cfg.s_hi, 1, "cpu")
+                sb = s.view(torch.int16).numpy().view(np.uint16)
+                t0 = time.perf_counter()
+                oracle.linear_from_bits(xb, name, p, sb, cfg.group_size, threads)
+                dt = time.perf_counter() - t0
+                if dt >= 0.2 * per_shape or rows >= N:
+                    break
+                rows = min(N, rows * 4)
+            done_bytes += rows * K // 4
+            spent += dt
+            rows_used[f"{N}x{K}@M{M}"] = rows
+    gbs = done_bytes / spent / 1e9 if spent > 0 else None
+    desc = (f"oracle fp64 C, {threads} threads: per (N,K) shape of {cfg.key} and every M in "
+            f"{list(Ms)}, a slice of output rows {rows_used}; {spent:.1f} s of CPU work; value = "
+            "packed bytes of the slices / CPU time")
+    return gbs, desc, spent
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="cfg2", choices=sorted(CONFIGS))
+    ap.add_argument("--ms", default="", help="comma list restricting M values")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of CPU oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    rank, world, local = dist_env()
+    cfg = CONFIGS[args.workload]
+    Ms = tuple(int(v) for v in args.ms.split(",")) if args.ms else cfg.Ms
+    threads = os.cpu_count() or 1
+    workload_name = (f"{cfg.key}: {cfg.title}; depth {cfg.depth}; "
+                     + ", ".join(f"{l.name} {l.N}x{l.K}" for l in cfg.layers) + f"; M in {list(Ms)}")
+    xdt = "bf16" if cfg.x_dtype == torch.bfloat16 else "f16"
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        # the oracle, as it stands, on a bounded sample per step
+        per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+        vals = []
+        for i in range(args.warmup + args.steps):
+            v, desc, spent = oracle_sample(cfg, Ms, per_step, threads)
+            if i >= args.warmup:
+                vals.append((v, spent))
+        value = statistics.median(v for v, _ in vals)
+        ms = statistics.median(s for _, s in vals) * 1e3
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": workload_name, "sample": desc},
+                "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import ternary_weight_linear_02_gb300 as tl
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        barrier = lambda: dist.barrier()  # noqa: E731
+    else:
+        barrier = lambda: None  # noqa: E731
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    tl.build()
+    tl.load()
+
+    stack = Stack(cfg, Ms, dev)
+    torch.cuda.synchronize()
+    # first call on the device outside capture (creates the status word)
+    stack.run_step(tl)
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))
+    g = capture(lambda: stack.run_step(tl), stream)
+
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    ms_total, t0, t1 = time_graph(g, stream, args.steps, args.warmup, barrier)
+    clocks.window(t0, t1)
+    clk = clocks.stop()
+    ms_step = ms_total / args.steps
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_step], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_step = float(tt.item())
+
+    pb = packed_bytes(cfg) * len(Ms)
+    ab = sum(algorithmic_bytes(cfg, M) for M in Ms)
+    value = world * pb / (ms_step * 1e-3) / 1e9
+    calls = stack.calls_per_step()
+    pk, pk_src = peaks()
+    peak = pk["hbm_gbs"]
+    achieved = ab / (ms_step * 1e-3) / 1e9  # all launches are the skinny kernel here
+    per_m = {}
+    for M in Ms:  # per-M decode-step time: time one M pass alone
+        gm = capture(lambda M=M: Stack.run_step(_OneM(stack, M), tl), stream)
+        mt, _, _ = time_graph(gm, stream, max(20, args.steps // 4), 3, lambda: None)
+        mt /= max(20, args.steps // 4)
+        per_m[str(M)] = {"us_per_decode_step": round(mt * 1e3, 2),
+                         "packed_GBps": round(packed_bytes(cfg) / (mt * 1e-3) / 1e9, 1),
+                         "frac_of_hbm": round(algorithmic_bytes(cfg, M) / (mt * 1e-3) / 1e9 / peak, 4),
+                         "eff_TFLOPs": round(flops(cfg, M) / (mt * 1e-3) / 1e12, 2)}
+        del gm
+
+    # end to end: pinned host x -> device, the calls, device out -> pinned host
+    e2e = None
+    if not args.no_e2e:
+        hx = {M: [[stack.x[M][d][j].cpu().pin_memory() for j in range(len(cfg.layers))]
+                  for d in range(cfg.depth)] for M in Ms}
+        ho = {M: [[torch.empty(stack.out[M][d][j].shape, dtype=cfg.x_dtype).pin_memory()
+                   for j in range(len(cfg.layers))] for d in range(cfg.depth)] for M in Ms}
+        h2d = sum(t.numel() * t.element_size() for M in Ms for r in hx[M] for t in r)
+        d2h = sum(t.numel() * t.element_size() for M in Ms for r in ho[M] for t in r)
+
+        def e2e_step():
+            for M in Ms:
+                for d in range(cfg.depth):
+                    for j in range(len(cfg.layers)):
+                        stack.x[M][d][j].copy_(hx[M][d][j], non_blocking=True)
+            stack.run_step(tl)
+            for M in Ms:
+                for d in range(cfg.depth):
+                    for j in range(len(cfg.layers)):
+                        ho[M][d][j].copy_(stack.out[M][d][j], non_blocking=True)
+
+        ge = capture(e2e_step, stream)
+        e_ms, _, _ = time_graph(ge, stream, args.steps, args.warmup, barrier)
+        e_step = e_ms / args.steps
+        if world > 1:
+            import torch.distributed as dist
+            tt = torch.tensor([e_step], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_step = float(tt.item())
+        e2e = {"value": world * pb / (e_step * 1e-3) / 1e9, "unit": "GB/s",
+               "ms_per_step": e_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del ge
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, desc, _ = oracle_sample(cfg, Ms, args.cpu_budget, threads)
+        cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    traffic = read_traffic(cfg.key)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": xdt, "data": "synthetic",
+        "config": {"workload": workload_name, "Ms": list(Ms), "calls_per_step": calls,
+                   "packed_bytes_per_step": pb, "algorithmic_bytes_per_step": ab,
+                   "l2": "inputs larger than L2: distinct per-layer weights, "
+                         f"{packed_bytes(cfg) / 1e9:.2f} GB packed per M pass",
+                   "per_M": per_m, "peaks_source": pk_src},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "skinny_mma_kernel (every launch of the step)",
+                     "peak_note": f"hbm_gbs of {pk_src} peaks"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": calls * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+class _OneM:
+    """A view of a Stack restricted to one M (for the per-M timings)."""
+
+    def __init__(self, stack, M):
+        self.cfg, self.Ms, self.w, self.x, self.out = stack.cfg, (M,), stack.w, stack.x, stack.out
+
+
+def read_traffic(key):
+    """Per-launch DRAM traffic from the committed ncu summary for this
+    workload, if its kernel fingerprint matches the current sources."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{key}.txt")
+    if not os.path.exists(path):
+        return None
+    want = None
+    vals = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    try:
+        from ternary_weight_linear_02_gb300 import _build
+        want = _build._fingerprint()[:16]
+    except Exception:
+        return None
+    if vals.get("kernel_fingerprint") != want:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,146 @@
+/*
+ * ternary_linear.h -- C ABI of libternary_gb300.so, a ternary-weight linear
+ * layer for NVIDIA GB300 (sm_103a).
+ *
+ * Format (all calls): a weight matrix W[N,K] with entries in {-1,0,+1} is
+ * stored packed as uint8 [N, K/4], row-major, K contiguous.  Weight k of row n
+ * is the 2-bit field (packed[n, k/4] >> 2*(k%4)) & 3 -- four weights per byte,
+ * little-endian, first weight in the lowest two bits -- with the code table
+ * 00 -> 0, 01 -> +1, 10 -> -1, 11 -> reserved, read as 0.
+ *   Source: "三元量化模型接入vLLM：从逆向加载到Kernel优化的完整实战"
+ *   (trdm.cn/news/729035) §2.2, §3.1; the Qwen2.5-7B ternary-in-vLLM write-up
+ *   (m.nxbn.cn/news/169761) §2.1, §2.2.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers named in the signature are DEVICE pointers (cudaMalloc'd or
+ *     otherwise device-accessible) unless stated otherwise.  The caller owns
+ *     every buffer; the library allocates nothing on these paths except one
+ *     4-byte device status word per device, created on the first call to
+ *     ternary_linear on that device (make that first call before any stream
+ *     capture).
+ *   - Arrays are dense row-major with no padding; pointers must be 16-byte
+ *     aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Work is enqueued asynchronously on it; no call synchronises.
+ *   - Argument errors are detected on the host before anything is enqueued; the
+ *     call then returns the error code and writes nothing.
+ *   - Launch failures return TL_ERR_CUDA (the CUDA error is cleared).
+ */
+#ifndef TERNARY_LINEAR_H
+#define TERNARY_LINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TL_OK = 0,
+    TL_ERR_NULL = 1,        /* a required pointer is NULL                        */
+    TL_ERR_SHAPE = 2,       /* negative size, K % 4 != 0, K % 128 != 0 in group
+                               mode, or a size beyond the supported range        */
+    TL_ERR_DTYPE = 3,       /* unknown dtype code or unsupported group size      */
+    TL_ERR_ALIGN = 4,       /* pointer not 16-byte aligned, or K % 64 != 0 for
+                               ternary_linear (packed rows must be 16-byte pitched) */
+    TL_ERR_VALUE = 5,       /* reserved for callers mapping a non-zero invalid /
+                               reserved count to an error                        */
+    TL_ERR_CUDA = 6,        /* a CUDA runtime call or a kernel launch failed     */
+    TL_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (see
+                               ternary_device_status)                            */
+    TL_ERR_UNSUPPORTED = 8  /* no sm_103 device current, or a path that cannot
+                               serve the arguments was forced                    */
+} tl_status;
+
+typedef enum { TL_F16 = 0, TL_BF16 = 1, TL_F32 = 2 } tl_dtype;
+
+/* Kernel path selection for ternary_linear_path. */
+typedef enum {
+    TL_PATH_AUTO = 0,    /* skinny path for M <= ternary_skinny_max_m(), else tile */
+    TL_PATH_SKINNY = 1,  /* fused decode + register-fed MMA GEMV / skinny GEMM     */
+    TL_PATH_TILE = 2     /* TMA + tcgen05 + TMEM tile GEMM                          */
+} tl_path;
+
+/*
+ * ternary_pack -- t [N,K] int8 in {-1,0,+1}  ->  packed [N,K/4] uint8.
+ *   Writes 00 for 0, 01 for +1, 10 for -1; never writes the reserved code 11.
+ *   ("三元量化模型接入vLLM…完整实战" §3.1.)
+ *   An entry outside {-1,0,+1} is written as 00 and counted.
+ *   invalid_count: device int64, may be NULL.  When non-NULL the library sets
+ *   it to zero on `stream` and then adds the number of invalid entries; read it
+ *   after synchronising `stream`.
+ *   Requires K % 4 == 0.  N == 0 or K == 0 enqueues only the count reset.
+ */
+tl_status ternary_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
+                       int64_t *invalid_count, void *stream);
+
+/*
+ * ternary_unpack -- packed [N,K/4] uint8  ->  t [N,K] int8 in {-1,0,+1}.
+ *   Bit-exact decode with the code table above; 11 decodes to 0 and is counted.
+ *   ("三元量化模型接入vLLM…完整实战" §3.1; Qwen2.5-7B write-up §2.2.)
+ *   reserved_count: device int64, may be NULL; reset to zero on `stream`, then
+ *   the number of 11 fields is added.
+ *   Requires K % 4 == 0.
+ */
+tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
+                         int64_t *reserved_count, void *stream);
+
+/*
+ * ternary_linear -- out[M,N] = x[M,K] * W^T with W = t * scale.
+ *   group_size == 0   : per-output-channel scale, scale is fp16 [N]
+ *                       out[m,n] = scale[n] * sum_k t[n,k] x[m,k]
+ *                       (Qwen2.5-7B write-up §3.2, §4.2)
+ *   group_size == 128 : per-(row, 128-wide K group) scale, scale is fp16 [N, K/128]
+ *                       out[m,n] = sum_g scale[n,g] * sum_{k in group g} t[n,k] x[m,k]
+ *                       ("三元量化模型接入vLLM…完整实战" §1.1, §3.1, §4.2)
+ *   x_dtype  : TL_F16 or TL_BF16.  scale is always fp16.
+ *   out_dtype: TL_F16, TL_BF16 or TL_F32.  Accumulation is fp32; a 16-bit
+ *              output is rounded to nearest even from fp32.
+ *   Sizes: M, N >= 0; K >= 0 with K % 64 == 0 (and K % 128 == 0 in group
+ *   mode).  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *   Fused layers (QKV, gate/up) are one call over the stacked rows: shard i
+ *   occupies rows [off_i, off_i + N_i) of packed and of scale, and columns
+ *   [off_i, off_i + N_i) of out.
+ *   Non-finite x is outside the contract.
+ */
+tl_status ternary_linear(const void *x, int32_t x_dtype, const uint8_t *packed,
+                         const void *scale, int32_t group_size, void *out,
+                         int32_t out_dtype, int64_t M, int64_t N, int64_t K,
+                         void *stream);
+
+/* Same as ternary_linear with an explicit kernel path (tl_path).  Returns
+ * TL_ERR_UNSUPPORTED if the forced path cannot serve the arguments (the
+ * skinny path serves M <= 32). */
+tl_status ternary_linear_path(const void *x, int32_t x_dtype, const uint8_t *packed,
+                              const void *scale, int32_t group_size, void *out,
+                              int32_t out_dtype, int64_t M, int64_t N, int64_t K,
+                              int32_t path, void *stream);
+
+/* Largest M the automatic dispatch sends to the skinny path (default 32,
+ * overridable with the environment variable TERNARY_SKINNY_MAX_M, read once). */
+int32_t ternary_skinny_max_m(void);
+
+/*
+ * ternary_device_status -- read (and optionally clear) the current device's
+ * status word.  Kernels whose waits are bounded write a non-zero code there
+ * when a wait gives up; *code receives TL_OK or TL_ERR_TIMEOUT.  Synchronous:
+ * call after the work in question has completed (e.g. after a stream sync).
+ */
+tl_status ternary_device_status(int32_t *code, int32_t clear);
+
+/* Human-readable name of a tl_status value (static storage, never NULL). */
+const char *ternary_status_string(int32_t status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t ternary_version(void);
+
+/* Testing aid (host only): the next n calls that pass argument validation
+ * return TL_ERR_CUDA without touching CUDA, as a failed launch would.  Lets
+ * error handling above the ABI be exercised without a GPU fault. */
+void ternary_test_inject_launch_failures(int32_t n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TERNARY_LINEAR_H */

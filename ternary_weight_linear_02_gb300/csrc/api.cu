@@ -1,0 +1,294 @@
+// api.cu -- the C ABI of libternary_gb300.so (declared in include/ternary_linear.h).
+//
+// Host-side duties only: argument validation (synchronous, before anything is
+// enqueued), per-device facts (SM count, architecture), the per-device status
+// word used by kernels with bounded waits, and the choice between the skinny
+// path (decode-shaped M) and the tcgen05 tile path.
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "ternary_linear.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+    bool init = false;
+    bool sm103 = false;
+    int sm_count = 0;
+    int *status = nullptr;  // 1 int, cudaMalloc'd on the first ternary_linear call
+};
+
+std::mutex g_mu;
+DevInfo g_dev[kMaxDevices];
+std::atomic<int> g_inject_launch_failures{0};
+
+int env_int(const char *name, int dflt) {
+    const char *v = std::getenv(name);
+    if (!v || !*v) return dflt;
+    return std::atoi(v);
+}
+
+int skinny_max_m() {
+    static const int v = [] {
+        int m = env_int("TERNARY_SKINNY_MAX_M", 32);
+        if (m < 0) m = 0;
+        if (m > 32) m = 32;
+        return m;
+    }();
+    return v;
+}
+
+bool pdl_enabled() {
+    static const bool v = env_int("TERNARY_PDL", 1) != 0;
+    return v;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Current device's facts; optionally make sure the status word exists.
+tl_status current_device(DevInfo **out, bool need_status) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return TL_ERR_CUDA;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return TL_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return TL_ERR_CUDA;
+        }
+        d.sm103 = (major == 10 && minor == 3);
+        d.sm_count = sms;
+        d.init = true;
+    }
+    if (!d.sm103) return TL_ERR_UNSUPPORTED;
+    if (need_status && d.status == nullptr) {
+        int *p = nullptr;
+        if (cudaMalloc(&p, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return TL_ERR_CUDA;
+        }
+        if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(p);
+            return TL_ERR_CUDA;
+        }
+        d.status = p;
+    }
+    *out = &d;
+    return TL_OK;
+}
+
+// Host-side fault injection for tests: the next n launch attempts fail with
+// TL_ERR_CUDA before touching the GPU.
+bool take_injected_failure() {
+    int n = g_inject_launch_failures.load();
+    while (n > 0) {
+        if (g_inject_launch_failures.compare_exchange_weak(n, n - 1)) return true;
+    }
+    return false;
+}
+
+tl_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return TL_OK;
+    cudaGetLastError();  // clear the sticky-free error state
+    return TL_ERR_CUDA;
+}
+
+size_t dtype_size(int32_t d) { return d == TL_F32 ? 4 : 2; }
+
+// Validation shared by ternary_linear / ternary_linear_path.  Returns TL_OK
+// and sets *noop when nothing needs to be enqueued.
+tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
+                       int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
+                       int64_t K, bool *noop) {
+    *noop = false;
+    if (x_dtype != TL_F16 && x_dtype != TL_BF16) return TL_ERR_DTYPE;
+    if (out_dtype != TL_F16 && out_dtype != TL_BF16 && out_dtype != TL_F32) return TL_ERR_DTYPE;
+    if (group_size != 0 && group_size != 128) return TL_ERR_DTYPE;
+    if (M < 0 || N < 0 || K < 0) return TL_ERR_SHAPE;
+    if (K % 4 != 0) return TL_ERR_SHAPE;
+    if (group_size == 128 && K % 128 != 0) return TL_ERR_SHAPE;
+    const int64_t lim = (int64_t)1 << 30;
+    if (M >= lim || N >= lim || K >= lim) return TL_ERR_SHAPE;
+    if (M == 0 || N == 0) {
+        *noop = true;
+        return TL_OK;
+    }
+    if (out == nullptr) return TL_ERR_NULL;
+    if (K > 0 && (x == nullptr || packed == nullptr)) return TL_ERR_NULL;
+    if (scale == nullptr && (group_size == 0 || K > 0)) return TL_ERR_NULL;
+    if (K % 64 != 0) return TL_ERR_ALIGN;
+    if (!aligned16(out) || (x && !aligned16(x)) || (packed && !aligned16(packed)) ||
+        (scale && !aligned16(scale)))
+        return TL_ERR_ALIGN;
+    return TL_OK;
+}
+
+tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
+                     int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
+                     int64_t K, int32_t path, void *stream) {
+    bool noop = false;
+    tl_status s = check_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
+                               &noop);
+    if (s != TL_OK || noop) return s;
+    if (path != TL_PATH_AUTO && path != TL_PATH_SKINNY && path != TL_PATH_TILE)
+        return TL_ERR_DTYPE;
+    if (take_injected_failure()) return TL_ERR_CUDA;
+    DevInfo *d = nullptr;
+    s = current_device(&d, true);
+    if (s != TL_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)(M * N) * dtype_size(out_dtype), st));
+
+    const bool bf = x_dtype == TL_BF16;
+    const bool group = group_size == 128;
+    tl::SkinnyPlan plan = tl::plan_skinny(M, N, K, d->sm_count);
+    const bool skinny_ok = plan.ok;
+    const bool tile_ok = tl::tile_supported(M, N, K);
+    int use = path;
+    if (use == TL_PATH_AUTO) {
+        use = (M <= skinny_max_m() && skinny_ok) ? TL_PATH_SKINNY : TL_PATH_TILE;
+        if (use == TL_PATH_TILE && !tile_ok && skinny_ok) use = TL_PATH_SKINNY;
+    }
+    if (use == TL_PATH_SKINNY) {
+        if (!skinny_ok) return TL_ERR_UNSUPPORTED;
+        tl::SkinnyArgs a{};
+        a.x = static_cast<const uint16_t *>(x);
+        a.packed = packed;
+        a.scale = static_cast<const uint16_t *>(scale);
+        a.out = out;
+        a.M = (int)M;
+        a.N = (int)N;
+        a.K = (int)K;
+        return from_cuda(tl::launch_skinny(a, bf, group, out_dtype, plan, st, pdl_enabled()));
+    }
+    if (!tile_ok) return TL_ERR_UNSUPPORTED;
+    tl::TileArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.packed = packed;
+    a.scale = static_cast<const uint16_t *>(scale);
+    a.out = out;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.status = d->status;
+    return from_cuda(tl::launch_tile(a, bf, group, out_dtype, d->sm_count, st, pdl_enabled()));
+}
+
+tl_status check_packing(const void *t, const void *packed, int64_t N, int64_t K,
+                        const int64_t *count) {
+    if (N < 0 || K < 0 || K % 4 != 0) return TL_ERR_SHAPE;
+    if (N >= ((int64_t)1 << 40) || K >= ((int64_t)1 << 40)) return TL_ERR_SHAPE;
+    if (N * K > 0 && (t == nullptr || packed == nullptr)) return TL_ERR_NULL;
+    if ((t && !aligned16(t)) || (packed && !aligned16(packed))) return TL_ERR_ALIGN;
+    if (count && (reinterpret_cast<uintptr_t>(count) & 7u)) return TL_ERR_ALIGN;
+    return TL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+tl_status ternary_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
+                       int64_t *invalid_count, void *stream) {
+    tl_status s = check_packing(t, packed, N, K, invalid_count);
+    if (s != TL_OK) return s;
+    if (take_injected_failure()) return TL_ERR_CUDA;
+    DevInfo *d = nullptr;
+    s = current_device(&d, false);
+    if (s != TL_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (invalid_count) {
+        s = from_cuda(cudaMemsetAsync(invalid_count, 0, sizeof(int64_t), st));
+        if (s != TL_OK) return s;
+    }
+    if (N * K == 0) return TL_OK;
+    return from_cuda(tl::launch_pack(t, packed, N * (K / 4),
+                                     reinterpret_cast<unsigned long long *>(invalid_count),
+                                     d->sm_count, st));
+}
+
+tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
+                         int64_t *reserved_count, void *stream) {
+    tl_status s = check_packing(t, packed, N, K, reserved_count);
+    if (s != TL_OK) return s;
+    if (take_injected_failure()) return TL_ERR_CUDA;
+    DevInfo *d = nullptr;
+    s = current_device(&d, false);
+    if (s != TL_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (reserved_count) {
+        s = from_cuda(cudaMemsetAsync(reserved_count, 0, sizeof(int64_t), st));
+        if (s != TL_OK) return s;
+    }
+    if (N * K == 0) return TL_OK;
+    return from_cuda(tl::launch_unpack(packed, t, N * (K / 4),
+                                       reinterpret_cast<unsigned long long *>(reserved_count),
+                                       d->sm_count, st));
+}
+
+tl_status ternary_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
+                         int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
+                         int64_t K, void *stream) {
+    return run_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
+                      TL_PATH_AUTO, stream);
+}
+
+tl_status ternary_linear_path(const void *x, int32_t x_dtype, const uint8_t *packed,
+                              const void *scale, int32_t group_size, void *out, int32_t out_dtype,
+                              int64_t M, int64_t N, int64_t K, int32_t path, void *stream) {
+    return run_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K, path,
+                      stream);
+}
+
+int32_t ternary_skinny_max_m(void) { return skinny_max_m(); }
+
+tl_status ternary_device_status(int32_t *code, int32_t clear) {
+    if (code == nullptr) return TL_ERR_NULL;
+    *code = TL_OK;
+    DevInfo *d = nullptr;
+    tl_status s = current_device(&d, false);
+    if (s != TL_OK) return s;
+    if (d->status == nullptr) return TL_OK;
+    int v = 0;
+    s = from_cuda(cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (s != TL_OK) return s;
+    if (v != 0) *code = TL_ERR_TIMEOUT;
+    if (clear && v != 0) s = from_cuda(cudaMemset(d->status, 0, sizeof(int)));
+    return s;
+}
+
+const char *ternary_status_string(int32_t status) {
+    switch (status) {
+    case TL_OK: return "TL_OK";
+    case TL_ERR_NULL: return "TL_ERR_NULL: a required pointer is NULL";
+    case TL_ERR_SHAPE: return "TL_ERR_SHAPE: invalid or unsupported sizes";
+    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size or path code";
+    case TL_ERR_ALIGN: return "TL_ERR_ALIGN: pointer not 16-byte aligned or K % 64 != 0";
+    case TL_ERR_VALUE: return "TL_ERR_VALUE: invalid or reserved values present";
+    case TL_ERR_CUDA: return "TL_ERR_CUDA: a CUDA call or kernel launch failed";
+    case TL_ERR_TIMEOUT: return "TL_ERR_TIMEOUT: a bounded device-side wait gave up";
+    case TL_ERR_UNSUPPORTED: return "TL_ERR_UNSUPPORTED: no sm_103 device, or the forced path "
+                                    "cannot serve these arguments";
+    default: return "unknown tl_status";
+    }
+}
+
+int32_t ternary_version(void) { return 100; }
+
+void ternary_test_inject_launch_failures(int32_t n) {
+    g_inject_launch_failures.store(n < 0 ? 0 : n);
+}
+
+}  // extern "C"

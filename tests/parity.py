@@ -1,0 +1,63 @@
+"""Shared helpers for the GPU parity tests: run the CUDA path through the
+binding and compare with the CPU oracle under the stated tolerance."""
+import numpy as np
+import torch
+
+import oracle
+
+# Tolerance (fp32 accumulation): relative L2 <= 1e-4 and per element
+# |err| <= 2e-3 * s_max(n) * sum_k |x[m,k]|.  A 16-bit output adds its own
+# rounding: half an ulp of the reference per element and the unit roundoff
+# to the relative L2 bound.
+REL_L2 = 1e-4
+PER_ELEM = 2e-3
+UNIT_ROUNDOFF = {torch.float32: 0.0, torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def x_dtype_name(dt: torch.dtype) -> str:
+    return {torch.float16: "f16", torch.bfloat16: "bf16"}[dt]
+
+
+def ulp(y: np.ndarray, dt: torch.dtype) -> np.ndarray:
+    if dt == torch.float32:
+        return np.zeros_like(y)
+    mant, emin = (10, -14) if dt == torch.float16 else (7, -126)
+    e = np.floor(np.log2(np.maximum(np.abs(y), 2.0 ** emin)))
+    return 2.0 ** (e - mant)
+
+
+def oracle_ref(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor, group_size: int,
+               rows=None, nthreads: int = 8) -> np.ndarray:
+    """Oracle output, optionally for a subset of output rows n (columns of y)."""
+    p = packed.detach().cpu().numpy()
+    s = bits(scale)
+    if rows is not None:
+        p = p[rows]
+        s = s[rows]
+    return oracle.linear_from_bits(bits(x), x_dtype_name(x.dtype), p, s, group_size, nthreads)
+
+
+def check(y_gpu: torch.Tensor, y_ref: np.ndarray, x: torch.Tensor, scale: torch.Tensor,
+          rows=None, what=""):
+    """Assert the documented tolerance; returns (rel_l2, max_ratio)."""
+    g = y_gpu.detach().float().cpu().numpy().astype(np.float64)
+    assert g.shape == y_ref.shape, (g.shape, y_ref.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    s = scale.detach().float().cpu().numpy().astype(np.float64)
+    if rows is not None:
+        s = s[rows]
+    smax = np.abs(s).reshape(s.shape[0], -1).max(axis=1)            # [N]
+    xabs = np.abs(x.detach().float().cpu().numpy().astype(np.float64)).sum(axis=1)  # [M]
+    bound = PER_ELEM * xabs[:, None] * smax[None, :] + 0.5 * ulp(y_ref, y_gpu.dtype)
+    err = np.abs(g - y_ref)
+    ratio = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    assert np.all(err <= bound), f"{what}: per-element bound exceeded (max ratio {ratio:.3g})"
+    den = float(np.linalg.norm(y_ref))
+    rel = float(np.linalg.norm(g - y_ref)) / den if den > 0 else float(np.linalg.norm(g))
+    lim = REL_L2 + UNIT_ROUNDOFF[y_gpu.dtype]
+    assert rel <= lim, f"{what}: relative L2 {rel:.3g} > {lim:.3g}"
+    return rel, ratio

@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer work (unpack, pack, counts) must be bit-exact; the linear layer must
+stay within the tolerance in tests/parity.py.  Inputs come from the seeded
+generator in ternary_weight_linear_02_gb300.synth; no expected value is
+produced by the CUDA path.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import ternary_weight_linear_02_gb300 as tl
+from ternary_weight_linear_02_gb300 import synth
+from ternary_weight_linear_02_gb300.workloads import CONFIGS
+
+from parity import check, oracle_ref
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    tl.build()
+    oracle.build()
+    tl.load()
+
+
+def layer_inputs(M, N, K, xdt, gs, seed, p_reserved=0.0, s_lo=0.005, s_hi=0.05):
+    x, p, s = synth.layer(M, N, K, xdt, gs, s_lo, s_hi, ("parity", seed, M, N, K, str(xdt), gs),
+                          "cpu", p_reserved)
+    return x.to(DEV), p.to(DEV), s.to(DEV)
+
+
+# ------------------------------------------------------------------ unpack / pack
+@pytest.mark.parametrize("N,K", [(1, 4), (3, 12), (7, 64), (33, 100), (256, 1024), (129, 4100),
+                                 (1000, 3584)])
+def test_unpack_bit_exact(N, K):
+    p = synth.packed_codes(N, K, synth.seed_for("unpack", N, K), "cpu", p_reserved=0.05)
+    t_ref, res_ref = oracle.unpack(p.numpy())
+    t, cnt = tl.unpack(p.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(t.cpu().numpy(), t_ref)
+    assert int(cnt.item()) == res_ref
+
+
+def test_unpack_all_bytes():
+    p = torch.arange(256, dtype=torch.uint8).reshape(64, 4)
+    t_ref, res_ref = oracle.unpack(p.numpy())
+    t, cnt = tl.unpack(p.to(DEV))
+    assert np.array_equal(t.cpu().numpy(), t_ref)
+    assert int(cnt.item()) == res_ref == 256
+
+
+@pytest.mark.parametrize("N,K", [(1, 4), (5, 24), (64, 256), (129, 4100), (1000, 3584)])
+def test_pack_bit_exact_and_invalid_count(N, K):
+    g = torch.Generator().manual_seed(N * 131 + K)
+    t = torch.randint(-1, 2, (N, K), dtype=torch.int8, generator=g)
+    bad = torch.rand((N, K), generator=g) < 0.01
+    t[bad] = torch.randint(2, 100, (int(bad.sum()),), generator=g, dtype=torch.int8)
+    p_ref, inv_ref = oracle.pack(t.numpy())
+    p, cnt = tl.pack(t.to(DEV))
+    assert np.array_equal(p.cpu().numpy(), p_ref)
+    assert int(cnt.item()) == inv_ref == int(bad.sum())
+
+
+def test_pack_unpack_roundtrip():
+    g = torch.Generator().manual_seed(3)
+    t = torch.randint(-1, 2, (300, 640), dtype=torch.int8, generator=g).to(DEV)
+    p, _ = tl.pack(t)
+    back, res = tl.unpack(p)
+    assert torch.equal(back, t)
+    assert int(res.item()) == 0
+
+
+# ------------------------------------------------------------------ linear, small
+SMALL = [
+    # M, N, K, x dtype, group size, out dtype
+    (1, 64, 128, torch.float16, 128, torch.float32),
+    (1, 70, 1152, torch.bfloat16, 0, torch.float32),
+    (1, 200, 64, torch.float16, 0, torch.float32),
+    (1, 1, 384, torch.bfloat16, 128, torch.float32),
+    (3, 129, 384, torch.bfloat16, 128, torch.bfloat16),
+    (4, 257, 192, torch.float16, 0, torch.float16),
+    (8, 96, 1024, torch.bfloat16, 0, torch.float32),
+    (9, 200, 640, torch.float16, 128, torch.float32),
+    (16, 131, 2048, torch.bfloat16, 128, torch.bfloat16),
+    (16, 64, 320, torch.bfloat16, 0, torch.float32),
+    (17, 100, 256, torch.float16, 0, torch.float16),
+    (24, 75, 1536, torch.bfloat16, 0, torch.float32),
+    (32, 300, 1024, torch.float16, 128, torch.float32),
+    (32, 64, 4096, torch.bfloat16, 128, torch.bfloat16),
+]
+
+
+@pytest.mark.parametrize("M,N,K,xdt,gs,odt", SMALL)
+def test_linear_skinny_small(M, N, K, xdt, gs, odt):
+    x, p, s = layer_inputs(M, N, K, xdt, gs, 1, p_reserved=0.01)
+    y = tl.linear(x, p, s, gs, out_dtype=odt, path="skinny")
+    torch.cuda.synchronize()
+    check(y, oracle_ref(x, p, s, gs), x, s, what=f"skinny {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("gs", [0, 128])
+@pytest.mark.parametrize("xdt", [torch.float16, torch.bfloat16])
+def test_linear_every_byte_exact(xdt, gs):
+    """Row n carries byte n in its first 4 weights (the rest 00); token 0 is
+    x = (1, 3, 9, 27, 0, ...), s = 1: y[0, n] is the balanced-ternary value of
+    the byte's four weights, an exact small integer."""
+    K = 128
+    p = torch.zeros((256, K // 4), dtype=torch.uint8)
+    p[:, 0] = torch.arange(256, dtype=torch.uint8)
+    x = torch.zeros((3, K), dtype=torch.float32)
+    x[0, :4] = torch.tensor([1.0, 3.0, 9.0, 27.0])
+    x[1, :4] = torch.tensor([-1.0, 0.5, 2.0, -4.0])
+    x[2] = torch.randn(K, generator=torch.Generator().manual_seed(0))
+    x = x.to(xdt)
+    s = torch.ones((256,) if gs == 0 else (256, K // 128), dtype=torch.float16)
+    want = oracle_ref(x, p, s, gs)
+    y = tl.linear(x.to(DEV), p.to(DEV), s.to(DEV), gs, out_dtype=torch.float32, path="skinny")
+    y = y.cpu().double().numpy()
+    assert np.array_equal(y[:2], want[:2])
+    np.testing.assert_allclose(y[2], want[2], rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("gs", [0, 128])
+def test_linear_closed_forms(gs):
+    M, K = 5, 512
+    rows = [0x55, 0xAA, 0x00, 0xFF]  # all +1, all -1, all 0, all reserved
+    p = torch.tensor([[r] * (K // 4) for r in rows], dtype=torch.uint8)
+    x = synth.activations(M, K, torch.bfloat16, 9)
+    s = torch.full((4,) if gs == 0 else (4, K // 128), 0.03125, dtype=torch.float16)
+    y = tl.linear(x.to(DEV), p.to(DEV), s.to(DEV), gs, out_dtype=torch.float32, path="skinny")
+    y = y.cpu().double()
+    xs = x.double().sum(1)
+    torch.testing.assert_close(y[:, 0], 0.03125 * xs, rtol=1e-5, atol=1e-6)
+    torch.testing.assert_close(y[:, 1], -0.03125 * xs, rtol=1e-5, atol=1e-6)
+    assert torch.all(y[:, 2] == 0) and torch.all(y[:, 3] == 0)
+
+
+def test_linear_three_d_input_and_k_zero():
+    x, p, s = layer_inputs(6, 40, 256, torch.bfloat16, 0, 2)
+    y = tl.linear(x.reshape(2, 3, 256), p, s)
+    assert y.shape == (2, 3, 40)
+    check(y.reshape(6, 40), oracle_ref(x, p, s, 0), x, s)
+    z = tl.linear(torch.empty((4, 0), dtype=torch.float16, device=DEV),
+                  torch.empty((8, 0), dtype=torch.uint8, device=DEV),
+                  torch.ones(8, dtype=torch.float16, device=DEV))
+    assert torch.count_nonzero(z) == 0
+
+
+def test_linear_deterministic():
+    x, p, s = layer_inputs(7, 3000, 4096, torch.bfloat16, 128, 4)
+    a = tl.linear(x, p, s, 128, out_dtype=torch.float32)
+    b = tl.linear(x, p, s, 128, out_dtype=torch.float32)
+    assert torch.equal(a, b)
+
+
+def test_linear_fused_shards_match_standalone():
+    M, K = 4, 3584
+    shards = [512, 128, 128]
+    parts = [layer_inputs(M, n, K, torch.bfloat16, 0, 10 + i) for i, n in enumerate(shards)]
+    x = parts[0][0]
+    p = torch.cat([q[1] for q in parts])
+    s = torch.cat([q[2] for q in parts])
+    ys = tl.linear_fused(x, p, s, shards, out_dtype=torch.float32)
+    for (xq, pq, sq), y in zip(parts, ys):
+        alone = tl.linear(x, pq, sq, out_dtype=torch.float32)
+        torch.testing.assert_close(y, alone, rtol=1e-5, atol=1e-6)
+
+
+def test_linear_graph_capture():
+    x, p, s = layer_inputs(4, 1024, 2048, torch.float16, 128, 5)
+    tl.linear(x, p, s, 128)  # first call on the device outside capture
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(st):
+        out = torch.empty((4, 1024), dtype=torch.float16, device=DEV)
+        with torch.cuda.graph(g, stream=st):
+            tl.linear(x, p, s, 128, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    check(out, oracle_ref(x, p, s, 128), x, s)
+
+
+# ------------------------------------------------------------------ full-size configs
+def sampled_rows(N, seed, k=48):
+    g = np.random.default_rng(seed)
+    rows = set(g.choice(N, size=min(k, N), replace=False).tolist())
+    rows |= {0, N - 1, N // 2}
+    return np.array(sorted(rows))
+
+
+SKINNY_FULL = [(c.key, l, M) for c in CONFIGS.values() for l in c.layers for M in c.Ms if M <= 32]
+
+
+@pytest.mark.parametrize("key,layer,M", SKINNY_FULL,
+                         ids=[f"{k}-{l.name}-M{M}" for k, l, M in SKINNY_FULL])
+def test_full_size_skinny_sampled(key, layer, M):
+    cfg = CONFIGS[key]
+    x, p, s = synth.layer(M, layer.N, layer.K, cfg.x_dtype, cfg.group_size, cfg.s_lo, cfg.s_hi,
+                          (key, layer.name, 0), DEV, cfg.p_reserved)
+    y = tl.linear(x, p, s, cfg.group_size, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rows = sampled_rows(layer.N, synth.seed_for(key, layer.name, M) & 0xFFFF)
+    ref = oracle_ref(x, p, s, cfg.group_size, rows=rows)
+    check(y[:, rows], ref, x, s, rows=rows, what=f"{key} {layer.name} M={M}")
