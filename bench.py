@@ -154,7 +154,7 @@ class Stack:
                 for j, l in enumerate(cfg.layers):
                     packed, scale = self.w[d][j]
                     tl.linear(self.x[M][d][j], packed, scale, cfg.group_size,
-                              out=self.out[M][d][j])
+                              out=self.out[M][d][j], static_weights=True)
 
 
 def capture(fn, stream):

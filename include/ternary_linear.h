@@ -108,13 +108,23 @@ tl_status ternary_linear(const void *x, int32_t x_dtype, const uint8_t *packed,
                          int32_t out_dtype, int64_t M, int64_t N, int64_t K,
                          void *stream);
 
-/* Same as ternary_linear with an explicit kernel path (tl_path).  Returns
- * TL_ERR_UNSUPPORTED if the forced path cannot serve the arguments (the
- * skinny path serves M <= 32). */
-tl_status ternary_linear_path(const void *x, int32_t x_dtype, const uint8_t *packed,
-                              const void *scale, int32_t group_size, void *out,
-                              int32_t out_dtype, int64_t M, int64_t N, int64_t K,
-                              int32_t path, void *stream);
+/* Flags for ternary_linear_ex. */
+typedef enum {
+    /* packed and scale are not written by any work still running on `stream`
+     * when this call's kernel starts (true for model weights loaded once).
+     * Lets the kernel read them before its stream predecessor has finished
+     * (programmatic dependent launch), overlapping consecutive layers. */
+    TL_FLAG_STATIC_WEIGHTS = 1
+} tl_flags;
+
+/* ternary_linear with an explicit kernel path (tl_path) and tl_flags bits.
+ * Returns TL_ERR_UNSUPPORTED if the forced path cannot serve the arguments
+ * (the skinny path serves M <= 32), TL_ERR_DTYPE for an unknown path or
+ * flag bit.  ternary_linear(...) == ternary_linear_ex(..., TL_PATH_AUTO, 0, stream). */
+tl_status ternary_linear_ex(const void *x, int32_t x_dtype, const uint8_t *packed,
+                            const void *scale, int32_t group_size, void *out,
+                            int32_t out_dtype, int64_t M, int64_t N, int64_t K,
+                            int32_t path, uint32_t flags, void *stream);
 
 /* Largest M the automatic dispatch sends to the skinny path (default 32,
  * overridable with the environment variable TERNARY_SKINNY_MAX_M, read once). */

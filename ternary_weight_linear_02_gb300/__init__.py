@@ -28,6 +28,7 @@ _lib = None
 
 TL_F16, TL_BF16, TL_F32 = 0, 1, 2
 PATHS = {"auto": 0, "skinny": 1, "tile": 2}
+FLAG_STATIC_WEIGHTS = 1
 _DT = {torch.float16: TL_F16, torch.bfloat16: TL_BF16, torch.float32: TL_F32}
 
 
@@ -61,8 +62,9 @@ def load():
     lib.ternary_pack.argtypes = [p, p, i64, i64, p, p]
     lib.ternary_unpack.argtypes = [p, p, i64, i64, p, p]
     lib.ternary_linear.argtypes = [p, i32, p, p, i32, p, i32, i64, i64, i64, p]
-    lib.ternary_linear_path.argtypes = [p, i32, p, p, i32, p, i32, i64, i64, i64, i32, p]
-    for f in (lib.ternary_pack, lib.ternary_unpack, lib.ternary_linear, lib.ternary_linear_path):
+    lib.ternary_linear_ex.argtypes = [p, i32, p, p, i32, p, i32, i64, i64, i64, i32,
+                                      ctypes.c_uint32, p]
+    for f in (lib.ternary_pack, lib.ternary_unpack, lib.ternary_linear, lib.ternary_linear_ex):
         f.restype = ctypes.c_int
     lib.ternary_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
     lib.ternary_device_status.restype = ctypes.c_int
@@ -136,12 +138,16 @@ def unpack(packed: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
 
 def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
            group_size: int | None = None, out_dtype: torch.dtype | None = None,
-           out: torch.Tensor | None = None, path: str = "auto") -> torch.Tensor:
+           out: torch.Tensor | None = None, path: str = "auto",
+           static_weights: bool = False) -> torch.Tensor:
     """out[..., N] = x[..., K] @ (t * scale)^T with t decoded from ``packed``.
 
     ``scale`` is fp16 [N] (per channel) or [N, K/128] (per 128-wide K group);
     ``group_size`` defaults from its rank.  Leading dimensions of ``x`` are
     flattened into M (the kernel takes a dense 2-D [M, K]).
+    ``static_weights=True`` promises that ``packed`` / ``scale`` are not being
+    written by work still running on the stream (TL_FLAG_STATIC_WEIGHTS), which
+    lets consecutive layers overlap.
     """
     _need_cuda(x, packed, scale, out)
     if x.dtype not in (torch.float16, torch.bfloat16):
@@ -152,8 +158,10 @@ def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
         raise ValueError("packed must be a 2-D uint8 tensor [N, K/4]")
     K = x.shape[-1]
     lead = x.shape[:-1]
-    x2 = x.reshape(-1, K).contiguous()
-    M = x2.shape[0]
+    M = 1
+    for d in lead:
+        M *= int(d)
+    x2 = x.reshape(M, K).contiguous()
     N = packed.shape[0]
     if packed.shape[1] * 4 != K:
         raise ValueError(f"packed is [N, {packed.shape[1]}] but K/4 = {K / 4}")
@@ -170,9 +178,9 @@ def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
     packed = packed.contiguous()
     scale = scale.contiguous()
     lib = load()
-    rc = lib.ternary_linear_path(_ptr(x2), _DT[x.dtype], _ptr(packed), _ptr(scale),
-                                 int(group_size), _ptr(out), _DT[odt], M, N, K, PATHS[path],
-                                 _stream(x.device))
+    rc = lib.ternary_linear_ex(_ptr(x2), _DT[x.dtype], _ptr(packed), _ptr(scale),
+                               int(group_size), _ptr(out), _DT[odt], M, N, K, PATHS[path],
+                               FLAG_STATIC_WEIGHTS if static_weights else 0, _stream(x.device))
     _check(rc, "ternary_linear")
     return out.reshape(*lead, N)
 

@@ -42,9 +42,23 @@ int skinny_max_m() {
     return v;
 }
 
+// Launch tuning knobs (environment, read once):
+//   TERNARY_PDL=0          launch without programmatic dependent launch
+//   TERNARY_PDL_TRIGGER=1  release dependents after the main loop instead of at entry
+//                      =2  no explicit release (dependents start when the grid exits)
+//   TERNARY_SKINNY_SK=n    force the skinny path's K split (cluster size), 0 = automatic
+//   TERNARY_L2_PREFETCH=0  no L2 bulk prefetch before griddepcontrol.wait
 bool pdl_enabled() {
     static const bool v = env_int("TERNARY_PDL", 1) != 0;
     return v;
+}
+
+int skinny_launch_flags(uint32_t api_flags) {
+    static const int trig = env_int("TERNARY_PDL_TRIGGER", 0);
+    static const int base = (trig == 1 ? tl::kSkinnyTriggerLate : 0) |
+                            (trig == 2 ? tl::kSkinnyTriggerNever : 0) |
+                            (env_int("TERNARY_L2_PREFETCH", 1) ? tl::kSkinnyPrefetchL2 : 0);
+    return base | ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kSkinnyStaticWeights : 0);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -137,13 +151,14 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
 
 tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
                      int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
-                     int64_t K, int32_t path, void *stream) {
+                     int64_t K, int32_t path, uint32_t flags, void *stream) {
     bool noop = false;
     tl_status s = check_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
                                &noop);
     if (s != TL_OK || noop) return s;
     if (path != TL_PATH_AUTO && path != TL_PATH_SKINNY && path != TL_PATH_TILE)
         return TL_ERR_DTYPE;
+    if (flags & ~(uint32_t)TL_FLAG_STATIC_WEIGHTS) return TL_ERR_DTYPE;
     if (take_injected_failure()) return TL_ERR_CUDA;
     DevInfo *d = nullptr;
     s = current_device(&d, true);
@@ -153,7 +168,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
 
     const bool bf = x_dtype == TL_BF16;
     const bool group = group_size == 128;
-    tl::SkinnyPlan plan = tl::plan_skinny(M, N, K, d->sm_count);
+    static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
+    tl::SkinnyPlan plan = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
     const bool skinny_ok = plan.ok;
     const bool tile_ok = tl::tile_supported(M, N, K);
     int use = path;
@@ -171,6 +187,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
         a.M = (int)M;
         a.N = (int)N;
         a.K = (int)K;
+        a.flags = skinny_launch_flags(flags);
+        a.status = d->status;
         return from_cuda(tl::launch_skinny(a, bf, group, out_dtype, plan, st, pdl_enabled()));
     }
     if (!tile_ok) return TL_ERR_UNSUPPORTED;
@@ -242,14 +260,15 @@ tl_status ternary_linear(const void *x, int32_t x_dtype, const uint8_t *packed, 
                          int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
                          int64_t K, void *stream) {
     return run_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
-                      TL_PATH_AUTO, stream);
+                      TL_PATH_AUTO, 0u, stream);
 }
 
-tl_status ternary_linear_path(const void *x, int32_t x_dtype, const uint8_t *packed,
-                              const void *scale, int32_t group_size, void *out, int32_t out_dtype,
-                              int64_t M, int64_t N, int64_t K, int32_t path, void *stream) {
+tl_status ternary_linear_ex(const void *x, int32_t x_dtype, const uint8_t *packed,
+                            const void *scale, int32_t group_size, void *out, int32_t out_dtype,
+                            int64_t M, int64_t N, int64_t K, int32_t path, uint32_t flags,
+                            void *stream) {
     return run_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K, path,
-                      stream);
+                      flags, stream);
 }
 
 int32_t ternary_skinny_max_m(void) { return skinny_max_m(); }

@@ -7,6 +7,12 @@
 // (same page §3.1).
 //
 // Design (memory-bound: every packed byte is read from HBM exactly once).
+//  * Work split: a CTA owns a block of RB = 16*TPC weight rows x KB of K
+//    (KB a multiple of 128).  Its packed rows are fetched as 1-D bulk async
+//    copies (one per row) into shared memory, all issued at kernel entry and
+//    tracked by one mbarrier.  With TL_FLAG_STATIC_WEIGHTS they are issued
+//    before griddepcontrol.wait, so under programmatic dependent launch a
+//    layer's weight stream runs while the previous kernel finishes.
 //  * The pages turn each +-1/0 product into add / subtract / skip on CUDA
 //    cores.  On GB300 that costs >= M adds per weight and saturates the ALUs
 //    long before HBM at M > 1, so here the decoded weight is fed to a warp MMA
@@ -24,14 +30,15 @@
 //    same permutation is applied to x when it is staged in shared memory), so
 //    each A register is one pair2() result and each B fragment one 8-byte
 //    shared load.
+//  * 8 warps per CTA: 8/TPC warps share each 16-row tile and split its K
+//    range; their partials are summed in a fixed order through shared memory.
 //  * Group scale: per-group fp32 partial in registers, folded into the total
 //    with s[n,g] at the group boundary.  Channel scale: once in the epilogue.
-//  * Split K across the CTAs of a thread-block cluster (<= 8); partial tiles
-//    are summed through distributed shared memory in rank order 0..SK-1, so
-//    the result is bit-identical run to run.  No global scratch.
-//  * The CTA's packed rows are bulk-prefetched into L2 before
-//    griddepcontrol.wait, so with programmatic dependent launch a layer's
-//    weight stream starts while the previous kernel in the stream finishes.
+//  * Split K across the CTAs of a thread-block cluster (<= 8): each CTA pushes
+//    its partial rows into the owning CTA's shared memory (distributed shared
+//    memory stores), one cluster barrier publishes them, and the owner sums
+//    them in rank order 0..SK-1, so the result is bit-identical run to run.
+//    No global scratch.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -59,240 +66,316 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
     }
 }
 
-// Slot of the staged x fragment for (group, word, step, n-tile, lane).  One
-// slot = 8 bytes = the B fragment {b0, b1} of one lane; the 32 lanes of a
-// (group, word, step, n-tile) read 256 contiguous bytes.
+// Slot of the staged x fragment for (group, word, step, n-tile, lane (g, t)).
+// One slot = 8 bytes = the B fragment {b0, b1} of one lane.  ts is the token
+// stride: 8, or M rounded up to a power of two when M < 8 (lanes of padding
+// tokens read nothing), so the lanes of one (group, word, step, n-tile) read
+// 32*ts contiguous bytes.
 template <int NT8>
-__device__ __forceinline__ int xslot(int grp, int w, int s, int nt, int t, int g) {
-    return ((((grp * 2 + w) * 4 + s) * NT8 + nt) * 4 + t) * 8 + g;
+__device__ __forceinline__ int xslot(int grp, int w, int s, int nt, int t, int g, int ts) {
+    return ((((grp * 2 + w) * 4 + s) * NT8 + nt) * 4 + t) * ts + g;
 }
 
-template <int NT8, int MT, int D, bool BF, bool GROUP, int OUT>
-__global__ void __launch_bounds__(kSkinnyThreads) skinny_mma_kernel(SkinnyArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    constexpr int RT = 16 * MT * (kSkinnyThreads / 32);  // rows per CTA
-    constexpr int MP = 8 * NT8;                          // padded tokens
+constexpr int kNW = kSkinnyWarps;
+
+template <int NT8, int TPC, bool BF, bool GROUP, int OUT>
+__global__ void __launch_bounds__(32 * kNW) skinny_mma_kernel(SkinnyArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int RB = 16 * TPC;     // rows per CTA
+    constexpr int KWS = kNW / TPC;   // warps per 16-row tile (split its K)
+    constexpr int MP = 8 * NT8;      // padded tokens
+    constexpr int NTH = 32 * kNW;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int n0 = blockIdx.x * RT;
+    const int n0 = blockIdx.x * RB;
     const int kb = blockIdx.y * a.kc;
     const int ke = min(a.K, kb + a.kc);
     const int klen = max(ke - kb, 0);
-    const int ng = (klen + 127) >> 7;  // groups in this CTA (the last may be half)
+    const int ng = (klen + 127) >> 7;  // 128-k groups of this CTA (the last may be half)
     const int64_t Kq = a.K >> 2;       // bytes per packed row
+    const int SK = gridDim.y;
+    const int valid_rows = max(0, min(RB, a.N - n0));
 
-    // 1. start this CTA's weight stream: bulk prefetch of its rows into L2
-    if (klen > 0) {
-        for (int r = threadIdx.x; r < RT; r += blockDim.x) {
-            const int n = n0 + r;
-            if (n < a.N) prefetch_l2_bulk(a.packed + (int64_t)n * Kq + (kb >> 2), klen >> 2);
-        }
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *codes = smem + 16;                                   // [RB][row_stride]
+    uint2 *xs = reinterpret_cast<uint2 *>(smem + a.x_off);        // fragment-ordered x
+    float *wpart = reinterpret_cast<float *>(smem + a.red_off);   // [kNW][16][MP]
+    float *recv = reinterpret_cast<float *>(smem + a.recv_off);   // [SK][rows_max][MP]
+
+    if (SK > 1) cluster_arrive_relaxed();  // cluster phase 1: this CTA runs
+    if (threadIdx.x == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
     }
-    pdl_launch_dependents();
-    pdl_wait();  // x / out may be produced / consumed by the previous kernel
+    __syncthreads();
 
-    // 2. stage x[:, kb:ke) in fragment order
-    uint2 *xs = reinterpret_cast<uint2 *>(smem);
-    {
-        const int units = MP * ng * 8;  // (token, group, t, word); 16 k each
-        for (int u = threadIdx.x; u < units; u += blockDim.x) {
-            const int w = u & 1, tt = (u >> 1) & 3, rest = u >> 3;
-            const int grp = rest % ng, m = rest / ng;
-            const int k = kb + grp * 128 + 32 * tt + 16 * w;
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-            if (m < a.M && k < ke) {
-                const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (int64_t)m * a.K + k);
-                lo = src[0];
-                hi = src[1];
-            }
-            const uint32_t W[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    // 1. weight stream: one bulk copy per packed row segment
+    auto issue_weights = [&]() {
+        if (warp == 0) {
+            const uint32_t row_bytes = (uint32_t)(klen >> 2);
+            if (lane == 0) mbar_arrive_expect_tx(bar, row_bytes * (uint32_t)valid_rows);
+            __syncwarp();
+            if (row_bytes > 0)
+                for (int r = lane; r < valid_rows; r += 32)
+                    bulk_g2s(codes + (size_t)r * a.row_stride,
+                             a.packed + (int64_t)(n0 + r) * Kq + (kb >> 2), row_bytes, bar);
+        }
+    };
+    const bool early_w = (a.flags & kSkinnyStaticWeights) != 0;
+    if (early_w) issue_weights();
+    if (!(a.flags & (kSkinnyTriggerLate | kSkinnyTriggerNever))) pdl_launch_dependents();
+    pdl_wait();  // x / out may be produced / consumed by the previous kernel
+    if (!early_w) issue_weights();
+
+    // per-channel scales of the outputs this thread stores (loaded early)
+    int rank = 0;
+    if (SK > 1) rank = (int)cg::this_cluster().block_rank();
+    const int r_begin = (RB * rank) / SK, r_end = (RB * (rank + 1)) / SK;
+    const int rows_mine = r_end - r_begin;
+    const int total = rows_mine * a.M;
+    constexpr int EPT = (RB * 32 + NTH - 1) / NTH;  // outputs per thread (M <= 32)
+    float osc[EPT];
 #pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                // slot s holds x at in-group offsets {s, s+8} (b0) and {s+4, s+12} (b1)
-                const uint32_t sel = (s & 1) ? 0x7632u : 0x5410u;
-                const uint32_t b0 = __byte_perm(W[s >> 1], W[(s >> 1) + 4], sel);
-                const uint32_t b1 = __byte_perm(W[(s >> 1) + 2], W[(s >> 1) + 6], sel);
-                xs[xslot<NT8>(grp, w, s, m >> 3, tt, m & 7)] = make_uint2(b0, b1);
+    for (int e = 0; e < EPT; ++e) {
+        const int idx = threadIdx.x + e * NTH;
+        const int n = n0 + r_begin + (idx < total ? idx % rows_mine : 0);
+        osc[e] = (!GROUP && idx < total && n < a.N) ? h2f(a.scale[n]) : 1.f;
+    }
+
+    // 2. stage x[:M, kb:ke) in fragment order (padding tokens are never read:
+    //    their lanes feed zero B fragments); one batch = one memory round trip
+    {
+        constexpr int UB = 4;
+        const int upm = ng * 8;  // units per token: (group, t, word), 16 k each
+        const int units = a.M * upm;
+        for (int base = 0; base < units; base += UB * NTH) {
+            uint4 lo[UB], hi[UB];
+#pragma unroll
+            for (int q = 0; q < UB; ++q) {
+                const int u = base + q * NTH + threadIdx.x;
+                lo[q] = make_uint4(0, 0, 0, 0);
+                hi[q] = lo[q];
+                if (u < units) {
+                    const int m = u / upm, r = u - m * upm;
+                    const int k = kb + (r >> 3) * 128 + 32 * ((r >> 1) & 3) + 16 * (r & 1);
+                    if (k < ke) {
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(a.x + (int64_t)m * a.K + k);
+                        lo[q] = src[0];
+                        hi[q] = src[1];
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < UB; ++q) {
+                const int u = base + q * NTH + threadIdx.x;
+                if (u < units) {
+                    const int m = u / upm, r = u - m * upm;
+                    const int grp = r >> 3, tt = (r >> 1) & 3, w = r & 1;
+                    const uint32_t W[8] = {lo[q].x, lo[q].y, lo[q].z, lo[q].w,
+                                           hi[q].x, hi[q].y, hi[q].z, hi[q].w};
+#pragma unroll
+                    for (int s = 0; s < 4; ++s) {
+                        // slot s holds x at in-group offsets {s, s+8} (b0), {s+4, s+12} (b1)
+                        const uint32_t sel = (s & 1) ? 0x7632u : 0x5410u;
+                        const uint32_t b0 = __byte_perm(W[s >> 1], W[(s >> 1) + 4], sel);
+                        const uint32_t b1 = __byte_perm(W[(s >> 1) + 2], W[(s >> 1) + 6], sel);
+                        xs[xslot<NT8>(grp, w, s, m >> 3, tt, m & 7, a.xts)] = make_uint2(b0, b1);
+                    }
+                }
             }
         }
     }
     __syncthreads();
 
-    // 3. main loop over the 128-k groups of this CTA
-    float acc[MT][NT8][4];
-    float accg[MT][NT8][4];
+    // 3. wait for this CTA's weights (bounded: a stuck copy sets the status
+    //    word and the CTA skips its work after one more bounded wait)
+    bool ok = mbar_wait_bounded(bar, 0);
+    if (!ok) {
+        if (a.status) atomicExch(a.status, kStatusTimeout);
+        mbar_wait_bounded(bar, 0);
+    }
+    ok = __syncthreads_and(ok);
+
+    // 4. main loop: warp -> (tile, K part); rows g and g+8 of the tile
+    const int tile = warp / KWS, kpart = warp % KWS;
+    const int gb = (ng * kpart) / KWS, ge = (ng * (kpart + 1)) / KWS;
+    constexpr int NC = (NT8 == 1) ? 2 : 1;  // independent MMA chains
+    float acc[NC][NT8][4];
+    float accg[NC][NT8][4];
 #pragma unroll
-    for (int i = 0; i < MT; ++i)
+    for (int c = 0; c < NC; ++c)
 #pragma unroll
         for (int j = 0; j < NT8; ++j)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
-
-    const uint8_t *rowp[MT][2];
-    const uint16_t *srow[MT][2];
-    bool rowok[MT][2];
+            for (int e = 0; e < 4; ++e) acc[c][j][e] = 0.f;
+    bool tok_ok[NT8];
+#pragma unroll
+    for (int j = 0; j < NT8; ++j) tok_ok[j] = (j * 8 + g) < a.M;
+    const int row_g = tile * 16 + g;
+    const uint8_t *cg0 = codes + (size_t)row_g * a.row_stride + 8 * t;
+    const uint8_t *cg8 = cg0 + (size_t)8 * a.row_stride;
     const int ngk = a.K >> 7;  // scale groups per row (group mode)
-#pragma unroll
-    for (int i = 0; i < MT; ++i)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int n = n0 + (warp * MT + i) * 16 + g + 8 * h;
-            rowok[i][h] = n < a.N;
-            const int nn = rowok[i][h] ? n : 0;
-            rowp[i][h] = a.packed + (int64_t)nn * Kq + (kb >> 2) + 8 * t;
-            srow[i][h] = a.scale + (GROUP ? (int64_t)nn * ngk + (kb >> 7) : 0);
-        }
+    const bool ok0 = n0 + row_g < a.N, ok8 = n0 + row_g + 8 < a.N;
+    const uint16_t *s0 = a.scale + (GROUP ? (int64_t)(ok0 ? n0 + row_g : 0) * ngk + (kb >> 7) : 0);
+    const uint16_t *s8 = a.scale + (GROUP ? (int64_t)(ok8 ? n0 + row_g + 8 : 0) * ngk + (kb >> 7) : 0);
 
-    uint2 ring[D][MT][2];
-    uint16_t sring[D][MT][2];
-    auto load_group = [&](int slot, int grp) {
-        const bool kin = grp < ng && (grp * 128 + 32 * t) < klen;
-#pragma unroll
-        for (int i = 0; i < MT; ++i)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                ring[slot][i][h] = (kin && rowok[i][h]) ? ldg_nc_v2(rowp[i][h] + grp * 32)
-                                                        : make_uint2(0, 0);
-                if constexpr (GROUP)
-                    sring[slot][i][h] = (grp < ng && rowok[i][h]) ? srow[i][h][grp] : (uint16_t)0;
+    uint16_t sn0 = 0, sn8 = 0;  // next group's scales (group mode)
+    if (GROUP && gb < ge) {
+        sn0 = ok0 ? s0[gb] : (uint16_t)0;
+        sn8 = ok8 ? s8[gb] : (uint16_t)0;
+    }
+    for (int grp = ok ? gb : ge; grp < ge; ++grp) {
+        const uint2 w0 = *reinterpret_cast<const uint2 *>(cg0 + grp * 32);
+        const uint2 w8 = *reinterpret_cast<const uint2 *>(cg8 + grp * 32);
+        float sc0 = 0.f, sc8 = 0.f;
+        if constexpr (GROUP) {
+            sc0 = h2f(sn0);
+            sc8 = h2f(sn8);
+            if (grp + 1 < ge) {
+                sn0 = ok0 ? s0[grp + 1] : (uint16_t)0;
+                sn8 = ok8 ? s8[grp + 1] : (uint16_t)0;
             }
-    };
 #pragma unroll
-    for (int d = 0; d < D; ++d) load_group(d, d);
-
-    for (int g0 = 0; g0 < ng; g0 += D) {
+            for (int c = 0; c < NC; ++c)
 #pragma unroll
-        for (int d = 0; d < D; ++d) {
-            const int grp = g0 + d;
-            if (grp < ng) {
-                uint2 cw[MT][2];
-                float sc[MT][2];
+                for (int j = 0; j < NT8; ++j)
 #pragma unroll
-                for (int i = 0; i < MT; ++i)
+                    for (int e = 0; e < 4; ++e) accg[c][j][e] = 0.f;
+        }
+        const uint2 *xg = xs + (size_t)grp * 32 * a.xts * NT8;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        cw[i][h] = ring[d][i][h];
-                        if constexpr (GROUP) sc[i][h] = h2f(sring[d][i][h]);
-                    }
-                load_group(d, grp + D);
-                if constexpr (GROUP) {
+        for (int w = 0; w < 2; ++w) {
+            const uint32_t zg = sign_nz(w ? w0.y : w0.x);
+            const uint32_t zh = sign_nz(w ? w8.y : w8.x);
 #pragma unroll
-                    for (int i = 0; i < MT; ++i)
+            for (int s = 0; s < 4; ++s) {
+                uint2 b[NT8];
 #pragma unroll
-                        for (int j = 0; j < NT8; ++j)
+                for (int j = 0; j < NT8; ++j)
+                    b[j] = tok_ok[j] ? xg[xslot<NT8>(0, w, s, j, t, g, a.xts)] : make_uint2(0, 0);
+                const uint32_t a0 = pair2(zg, s), a1 = pair2(zh, s);
+                const uint32_t a2 = pair2(zg, s + 4), a3 = pair2(zh, s + 4);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) accg[i][j][e] = 0.f;
+                for (int j = 0; j < NT8; ++j) {
+                    if constexpr (GROUP)
+                        mma16816<BF>(accg[s % NC][j], a0, a1, a2, a3, b[j].x, b[j].y);
+                    else
+                        mma16816<BF>(acc[s % NC][j], a0, a1, a2, a3, b[j].x, b[j].y);
                 }
+            }
+        }
+        if constexpr (GROUP) {
 #pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    uint32_t zg[MT], zh[MT];
+            for (int j = 0; j < NT8; ++j) {
+                float p[4];
 #pragma unroll
-                    for (int i = 0; i < MT; ++i) {
-                        zg[i] = sign_nz(w ? cw[i][0].y : cw[i][0].x);
-                        zh[i] = sign_nz(w ? cw[i][1].y : cw[i][1].x);
-                    }
-#pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        uint2 b[NT8];
-#pragma unroll
-                        for (int j = 0; j < NT8; ++j) b[j] = xs[xslot<NT8>(grp, w, s, j, t, g)];
-#pragma unroll
-                        for (int i = 0; i < MT; ++i) {
-                            const uint32_t a0 = pair2(zg[i], s), a1 = pair2(zh[i], s);
-                            const uint32_t a2 = pair2(zg[i], s + 4), a3 = pair2(zh[i], s + 4);
-#pragma unroll
-                            for (int j = 0; j < NT8; ++j) {
-                                if constexpr (GROUP)
-                                    mma16816<BF>(accg[i][j], a0, a1, a2, a3, b[j].x, b[j].y);
-                                else
-                                    mma16816<BF>(acc[i][j], a0, a1, a2, a3, b[j].x, b[j].y);
-                            }
-                        }
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    p[e] = accg[0][j][e];
+                    if constexpr (NC == 2) p[e] += accg[NC - 1][j][e];
                 }
-                if constexpr (GROUP) {
-#pragma unroll
-                    for (int i = 0; i < MT; ++i)
-#pragma unroll
-                        for (int j = 0; j < NT8; ++j) {
-                            acc[i][j][0] = fmaf(sc[i][0], accg[i][j][0], acc[i][j][0]);
-                            acc[i][j][1] = fmaf(sc[i][0], accg[i][j][1], acc[i][j][1]);
-                            acc[i][j][2] = fmaf(sc[i][1], accg[i][j][2], acc[i][j][2]);
-                            acc[i][j][3] = fmaf(sc[i][1], accg[i][j][3], acc[i][j][3]);
-                        }
-                }
+                acc[0][j][0] = fmaf(sc0, p[0], acc[0][j][0]);
+                acc[0][j][1] = fmaf(sc0, p[1], acc[0][j][1]);
+                acc[0][j][2] = fmaf(sc8, p[2], acc[0][j][2]);
+                acc[0][j][3] = fmaf(sc8, p[3], acc[0][j][3]);
             }
         }
     }
+    if (a.flags & kSkinnyTriggerLate) pdl_launch_dependents();
+    if constexpr (!GROUP && NC == 2) {
+#pragma unroll
+        for (int j = 0; j < NT8; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[0][j][e] += acc[NC - 1][j][e];
+    }
 
-    // 4. partial tile -> shared memory, [RT rows][MP tokens] fp32
-    __syncthreads();  // x fragments are no longer needed; reuse the space
-    float *part = reinterpret_cast<float *>(smem);
+    // 5. warp partials -> shared memory; the KWS warps of a tile are summed
+    //    in a fixed order into the slot of the tile's first warp.  The CTA
+    //    partial of row r then lives at part(r) below.
 #pragma unroll
-    for (int i = 0; i < MT; ++i)
+    for (int h = 0; h < 2; ++h) {
+        float *dst = wpart + ((size_t)warp * 16 + g + 8 * h) * MP;
 #pragma unroll
-        for (int j = 0; j < NT8; ++j) {
-            const int r = (warp * MT + i) * 16 + g;
-            *reinterpret_cast<float2 *>(&part[r * MP + j * 8 + 2 * t]) =
-                make_float2(acc[i][j][0], acc[i][j][1]);
-            *reinterpret_cast<float2 *>(&part[(r + 8) * MP + j * 8 + 2 * t]) =
-                make_float2(acc[i][j][2], acc[i][j][3]);
+        for (int j = 0; j < NT8; ++j)
+            *reinterpret_cast<float2 *>(dst + j * 8 + 2 * t) =
+                make_float2(acc[0][j][2 * h], acc[0][j][2 * h + 1]);
+    }
+    auto part = [&](int r) { return wpart + ((size_t)(r >> 4) * KWS * 16 + (r & 15)) * MP; };
+    if constexpr (KWS > 1) {
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < RB * MP; idx += NTH) {
+            const int r = idx / MP, m = idx - r * MP;
+            const float *src = part(r) + m;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < KWS; ++w) v += src[(size_t)w * 16 * MP];
+            part(r)[m] = v;  // element read and written by this thread only
         }
+    }
 
-    // 5. split-K reduction across the cluster (rank order), scale, store
-    const int SK = gridDim.y;
-    int rank = 0;
+    // 6. split-K across the cluster: push each row's CTA partial into slot
+    //    `rank` of the owning CTA's receive buffer; one cluster barrier
+    //    publishes them.  Rank q owns rows [RB*q/SK, RB*(q+1)/SK).
+    const int rows_max = (RB + SK - 1) / SK;
     if (SK > 1) {
         cg::cluster_group cluster = cg::this_cluster();
+        if constexpr (KWS == 1) __syncthreads();
+        cluster_wait();  // every CTA of the cluster has started
+        for (int idx = threadIdx.x; idx < RB * MP; idx += NTH) {
+            const int r = idx / MP, m = idx - r * MP;
+            int o = (r * SK) / RB;
+            while (o > 0 && r < (RB * o) / SK) --o;
+            while (o + 1 < SK && r >= (RB * (o + 1)) / SK) ++o;
+            cluster.map_shared_rank(recv, o)[((size_t)rank * rows_max + (r - (RB * o) / SK)) * MP + m] =
+                part(r)[m];
+        }
         cluster.sync();
-        rank = (int)cluster.block_rank();
     } else {
         __syncthreads();
     }
-    const int r_begin = (RT * rank) / SK, r_end = (RT * (rank + 1)) / SK;
-    const int rows_mine = r_end - r_begin;
-    const int total = rows_mine * a.M;
-    for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
-        const int r = r_begin + idx % rows_mine;
+
+    // 7. sum the CTA partials in rank order, scale, convert, store
+#pragma unroll
+    for (int e = 0; e < EPT; ++e) {
+        const int idx = threadIdx.x + e * NTH;
+        if (idx >= total) break;
+        const int rr = idx % rows_mine;
         const int m = idx / rows_mine;
-        const int n = n0 + r;
-        if (n >= a.N) continue;
+        const int n = n0 + r_begin + rr;
+        if (n >= a.N || !ok) continue;
         float v = 0.f;
         if (SK > 1) {
-            cg::cluster_group cluster = cg::this_cluster();
-            for (int q = 0; q < SK; ++q) v += cluster.map_shared_rank(part, q)[r * MP + m];
+            for (int q = 0; q < SK; ++q) v += recv[((size_t)q * rows_max + rr) * MP + m];
         } else {
-            v = part[r * MP + m];
+            v = part(rr)[m];
         }
         v *= 0.5f;  // the decoded operand is 2*t
-        if constexpr (!GROUP) v *= h2f(a.scale[n]);
+        if constexpr (!GROUP) v *= osc[e];
         OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, v);
     }
-    if (SK > 1) cg::this_cluster().sync();  // keep our partials alive for readers
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
-template <int NT8, int MT, bool BF, bool GROUP, int OUT>
-static cudaError_t launch_cfg(const SkinnyArgs &a, int rows_per_cta, int sk, size_t smem,
-                              cudaStream_t st, bool pdl) {
-    constexpr int D = (MT == 1) ? 4 : 2;
-    auto kern = skinny_mma_kernel<NT8, MT, D, BF, GROUP, OUT>;
+template <int NT8, int TPC, bool BF, bool GROUP, int OUT>
+static cudaError_t launch_cfg(const SkinnyArgs &a, const SkinnyPlan &p, cudaStream_t st,
+                              bool pdl) {
+    auto kern = skinny_mma_kernel<NT8, TPC, BF, GROUP, OUT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+                                         (int)p.smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.N + rows_per_cta - 1) / rows_per_cta), (unsigned)sk, 1);
-    cfg.blockDim = dim3(kSkinnyThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
+    cfg.gridDim = dim3((unsigned)((a.N + p.rows_per_cta - 1) / p.rows_per_cta), (unsigned)p.sk, 1);
+    cfg.blockDim = dim3(32 * kNW, 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     int na = 0;
-    if (sk > 1) {
+    if (p.sk > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
         attr[na].val.clusterDim.x = 1;
-        attr[na].val.clusterDim.y = (unsigned)sk;
+        attr[na].val.clusterDim.y = (unsigned)p.sk;
         attr[na].val.clusterDim.z = 1;
         ++na;
     }
@@ -306,54 +389,90 @@ static cudaError_t launch_cfg(const SkinnyArgs &a, int rows_per_cta, int sk, siz
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <int NT8, int MT, bool BF, bool GROUP>
-static cudaError_t dispatch_out(const SkinnyArgs &a, int out_dtype, int rpc, int sk, size_t smem,
+template <int NT8, int TPC, bool BF, bool GROUP>
+static cudaError_t dispatch_out(const SkinnyArgs &a, int out_dtype, const SkinnyPlan &p,
                                 cudaStream_t st, bool pdl) {
     switch (out_dtype) {
-    case 0: return launch_cfg<NT8, MT, BF, GROUP, 0>(a, rpc, sk, smem, st, pdl);
-    case 1: return launch_cfg<NT8, MT, BF, GROUP, 1>(a, rpc, sk, smem, st, pdl);
-    default: return launch_cfg<NT8, MT, BF, GROUP, 2>(a, rpc, sk, smem, st, pdl);
+    case 0: return launch_cfg<NT8, TPC, BF, GROUP, 0>(a, p, st, pdl);
+    case 1: return launch_cfg<NT8, TPC, BF, GROUP, 1>(a, p, st, pdl);
+    default: return launch_cfg<NT8, TPC, BF, GROUP, 2>(a, p, st, pdl);
     }
 }
 
-template <int NT8, int MT>
+template <int NT8, int TPC>
 static cudaError_t dispatch_types(const SkinnyArgs &a, bool bf, bool group, int out_dtype,
-                                  int rpc, int sk, size_t smem, cudaStream_t st, bool pdl) {
-    if (bf) {
-        return group ? dispatch_out<NT8, MT, true, true>(a, out_dtype, rpc, sk, smem, st, pdl)
-                     : dispatch_out<NT8, MT, true, false>(a, out_dtype, rpc, sk, smem, st, pdl);
-    }
-    return group ? dispatch_out<NT8, MT, false, true>(a, out_dtype, rpc, sk, smem, st, pdl)
-                 : dispatch_out<NT8, MT, false, false>(a, out_dtype, rpc, sk, smem, st, pdl);
+                                  const SkinnyPlan &p, cudaStream_t st, bool pdl) {
+    if (bf)
+        return group ? dispatch_out<NT8, TPC, true, true>(a, out_dtype, p, st, pdl)
+                     : dispatch_out<NT8, TPC, true, false>(a, out_dtype, p, st, pdl);
+    return group ? dispatch_out<NT8, TPC, false, true>(a, out_dtype, p, st, pdl)
+                 : dispatch_out<NT8, TPC, false, false>(a, out_dtype, p, st, pdl);
 }
 
-SkinnyPlan plan_skinny(int64_t M, int64_t N, int64_t K, int sm_count) {
+template <int NT8>
+static cudaError_t dispatch_tpc(const SkinnyArgs &a, bool bf, bool group, int out_dtype,
+                                const SkinnyPlan &p, cudaStream_t st, bool pdl) {
+    switch (p.rows_per_cta / 16) {
+    case 1: return dispatch_types<NT8, 1>(a, bf, group, out_dtype, p, st, pdl);
+    case 2: return dispatch_types<NT8, 2>(a, bf, group, out_dtype, p, st, pdl);
+    case 4: return dispatch_types<NT8, 4>(a, bf, group, out_dtype, p, st, pdl);
+    default: return dispatch_types<NT8, 8>(a, bf, group, out_dtype, p, st, pdl);
+    }
+}
+
+static SkinnyPlan make_plan(int64_t M, int64_t N, int64_t K, int64_t rb, int64_t sk) {
     SkinnyPlan p{};
     p.nt8 = M <= 8 ? 1 : (M <= 16 ? 2 : 4);
-    p.mt = p.nt8 == 1 ? 1 : 2;
-    p.rows_per_cta = 16 * p.mt * (kSkinnyThreads / 32);
-    const int64_t row_tiles = (N + p.rows_per_cta - 1) / p.rows_per_cta;
-    const int64_t ngk = (K + 127) / 128;  // 128-k groups (last may be half)
-    const int64_t want_ctas = 2LL * sm_count;
-    int64_t sk = (want_ctas + row_tiles - 1) / row_tiles;
+    p.rows_per_cta = (int)rb;
+    const int64_t G = (K + 127) / 128;  // 128-k groups (last may be half)
     if (sk > kSkinnyMaxCluster) sk = kSkinnyMaxCluster;
-    if (sk > ngk) sk = ngk;
+    if (sk > G) sk = G;
     if (sk < 1) sk = 1;
-    int64_t gpc = (ngk + sk - 1) / sk;  // groups per CTA
-    // shared memory: x fragments (2048 B per group per n-tile) or the partial tile
-    const int64_t per_group = 2048LL * p.nt8;
-    while (gpc * per_group > kSkinnyMaxSmem && sk < kSkinnyMaxCluster) {
-        ++sk;
-        gpc = (ngk + sk - 1) / sk;
-    }
-    sk = (ngk + gpc - 1) / gpc;  // no CTA without work
-    if (sk < 1) sk = 1;
+    const int64_t gpc = (G + sk - 1) / sk;  // groups per CTA
+    sk = (G + gpc - 1) / gpc;               // no CTA without work
+    const int64_t mp = 8LL * p.nt8;
+    int64_t ts = 8;
+    if (M < 8) ts = M <= 1 ? 1 : (M <= 2 ? 2 : (M <= 4 ? 4 : 8));
+    p.xts = (int)ts;
+    const int64_t row_stride = 32 * (gpc | 1);  // odd multiple of 32 B: conflict-free reads
+    const int64_t codes = rb * row_stride;
+    const int64_t xbytes = gpc * 256LL * ts * p.nt8;  // 8 slots of 8 B per (word, step, t)
+    const int64_t wbytes = (int64_t)kNW * 16 * mp * 4;
+    const int64_t rows_max = (rb + sk - 1) / sk;
+    const int64_t rbytes = sk > 1 ? sk * rows_max * mp * 4 : 0;
     p.sk = (int)sk;
     p.kc = (int)(gpc * 128);
-    const int64_t xbytes = gpc * per_group;
-    const int64_t pbytes = (int64_t)p.rows_per_cta * 8 * p.nt8 * 4;
-    p.smem = (size_t)(xbytes > pbytes ? xbytes : pbytes);
-    p.ok = xbytes <= kSkinnyMaxSmem && M <= 32;
+    p.row_stride = (int)row_stride;
+    p.x_off = (int)(16 + codes);
+    p.red_off = (int)(16 + codes + xbytes);
+    p.recv_off = (int)(16 + codes + xbytes + wbytes);
+    p.smem = (size_t)(16 + codes + xbytes + wbytes + rbytes);
+    p.ok = (int64_t)p.smem <= kSkinnyMaxSmem && M <= 32 && M >= 1;
+    return p;
+}
+
+SkinnyPlan plan_skinny(int64_t M, int64_t N, int64_t K, int sm_count, int force_sk) {
+    // Rows per CTA: large enough that the staged x slice (2*M bytes per k) is
+    // small next to the weight slice (RB/4 bytes per k), capped at 128.
+    int64_t rb = 16;
+    while (rb < 128 && rb < 16 * M) rb *= 2;
+    const int64_t G = (K + 127) / 128;
+    auto choose_sk = [&](int64_t rbv) {
+        const int64_t R = (N + rbv - 1) / rbv;
+        int64_t sk = R >= sm_count ? 1 : (sm_count + R - 1) / R;
+        if (force_sk > 0) sk = force_sk;
+        return sk;
+    };
+    SkinnyPlan p = make_plan(M, N, K, rb, choose_sk(rb));
+    // keep one CTA within the budget that lets two CTAs share an SM
+    while (p.smem > (size_t)kSkinnyTargetSmem && p.sk < kSkinnyMaxCluster && p.sk < G)
+        p = make_plan(M, N, K, rb, p.sk + 1);
+    while ((!p.ok || p.smem > (size_t)kSkinnyTargetSmem) && rb > 16) {
+        rb /= 2;
+        p = make_plan(M, N, K, rb, choose_sk(rb));
+        while (p.smem > (size_t)kSkinnyTargetSmem && p.sk < kSkinnyMaxCluster && p.sk < G)
+            p = make_plan(M, N, K, rb, p.sk + 1);
+    }
     return p;
 }
 
@@ -361,11 +480,14 @@ cudaError_t launch_skinny(const SkinnyArgs &a, bool bf, bool group, int out_dtyp
                           const SkinnyPlan &p, cudaStream_t st, bool pdl) {
     SkinnyArgs b = a;
     b.kc = p.kc;
-    switch (p.nt8) {
-    case 1: return dispatch_types<1, 1>(b, bf, group, out_dtype, p.rows_per_cta, p.sk, p.smem, st, pdl);
-    case 2: return dispatch_types<2, 2>(b, bf, group, out_dtype, p.rows_per_cta, p.sk, p.smem, st, pdl);
-    default: return dispatch_types<4, 2>(b, bf, group, out_dtype, p.rows_per_cta, p.sk, p.smem, st, pdl);
-    }
+    b.row_stride = p.row_stride;
+    b.x_off = p.x_off;
+    b.red_off = p.red_off;
+    b.recv_off = p.recv_off;
+    b.xts = p.xts;
+    if (p.nt8 == 1) return dispatch_tpc<1>(b, bf, group, out_dtype, p, st, pdl);
+    if (p.nt8 == 2) return dispatch_tpc<2>(b, bf, group, out_dtype, p, st, pdl);
+    return dispatch_tpc<4>(b, bf, group, out_dtype, p, st, pdl);
 }
 
 }  // namespace tl

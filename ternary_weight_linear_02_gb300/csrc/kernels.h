@@ -15,9 +15,16 @@ cudaError_t launch_pack(const int8_t *t, uint8_t *packed, int64_t nbytes,
                         unsigned long long *invalid, int sm_count, cudaStream_t st);
 
 // ------------------------------------------------------------ skinny path
-constexpr int kSkinnyThreads = 128;        // 4 warps, 16*MT rows each
+constexpr int kSkinnyWarps = 8;            // warps per CTA
 constexpr int kSkinnyMaxCluster = 8;       // portable cluster size
 constexpr int64_t kSkinnyMaxSmem = 200 * 1024;
+constexpr int64_t kSkinnyTargetSmem = 100 * 1024;  // two CTAs per SM (overlap of layers)
+
+// SkinnyArgs::flags
+constexpr int kSkinnyStaticWeights = 1;  // packed/scale may be read before griddepcontrol.wait
+constexpr int kSkinnyTriggerLate = 2;    // launch dependents after the main loop, not at entry
+constexpr int kSkinnyPrefetchL2 = 4;     // bulk-prefetch the CTA's packed rows into L2 at entry
+constexpr int kSkinnyTriggerNever = 8;   // no explicit trigger (dependents start at exit)
 
 struct SkinnyArgs {
     const uint16_t *x;       // [M,K] fp16 or bf16 bits
@@ -26,19 +33,30 @@ struct SkinnyArgs {
     void *out;               // [M,N]
     int M, N, K;
     int kc;                  // k per CTA (multiple of 128), set from the plan
+    int row_stride;          // shared-memory bytes per staged packed row
+    int x_off;               // byte offsets in shared memory: staged x fragments,
+    int red_off;             //   per-warp partial tiles,
+    int recv_off;            //   split-K receive buffer
+    int flags;               // kSkinny* bits
+    int xts;                 // token stride of the staged x fragments (1, 2, 4 or 8)
+    int *status;             // device status word (bounded-wait failures)
 };
 
 struct SkinnyPlan {
     int nt8;           // 8-token MMA tiles
-    int mt;            // 16-row MMA tiles per warp
-    int rows_per_cta;
+    int rows_per_cta;  // 16, 32, 64 or 128
     int sk;            // K split = cluster size
     int kc;            // k per CTA
+    int row_stride;
+    int x_off;
+    int xts;
     size_t smem;
+    int red_off;
+    int recv_off;
     bool ok;
 };
 
-SkinnyPlan plan_skinny(int64_t M, int64_t N, int64_t K, int sm_count);
+SkinnyPlan plan_skinny(int64_t M, int64_t N, int64_t K, int sm_count, int force_sk = 0);
 cudaError_t launch_skinny(const SkinnyArgs &a, bool bf, bool group, int out_dtype,
                           const SkinnyPlan &p, cudaStream_t st, bool pdl);
 

@@ -66,10 +66,11 @@ def test_status_strings(lib):
     assert lib.ternary_version() >= 100
 
 
-def lin(lib, x=A, xdt=0, packed=B, scale=C, gs=0, out=D, odt=2, M=4, N=8, K=128, path=0):
-    return lib.ternary_linear_path(ctypes.c_void_p(x), xdt, ctypes.c_void_p(packed),
-                                   ctypes.c_void_p(scale), gs, ctypes.c_void_p(out), odt, M, N,
-                                   K, path, None)
+def lin(lib, x=A, xdt=0, packed=B, scale=C, gs=0, out=D, odt=2, M=4, N=8, K=128, path=0,
+        flags=0):
+    return lib.ternary_linear_ex(ctypes.c_void_p(x), xdt, ctypes.c_void_p(packed),
+                                 ctypes.c_void_p(scale), gs, ctypes.c_void_p(out), odt, M, N,
+                                 K, path, flags, None)
 
 
 def test_linear_argument_errors(lib):
@@ -78,6 +79,7 @@ def test_linear_argument_errors(lib):
     assert lin(lib, odt=5) == TL_ERR_DTYPE
     assert lin(lib, gs=64) == TL_ERR_DTYPE
     assert lin(lib, path=7) == TL_ERR_DTYPE
+    assert lin(lib, flags=2) == TL_ERR_DTYPE
     assert lin(lib, M=-1) == TL_ERR_SHAPE
     assert lin(lib, N=-2) == TL_ERR_SHAPE
     assert lin(lib, K=130) == TL_ERR_SHAPE           # K % 4

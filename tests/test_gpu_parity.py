@@ -153,6 +153,16 @@ def test_linear_three_d_input_and_k_zero():
     assert torch.count_nonzero(z) == 0
 
 
+@pytest.mark.parametrize("M", [1, 12])
+def test_linear_static_weights_flag(M):
+    """TL_FLAG_STATIC_WEIGHTS only changes when weights are read, not results."""
+    x, p, s = layer_inputs(M, 4096, 4096, torch.bfloat16, 0, 6)
+    a = tl.linear(x, p, s, 0, out_dtype=torch.float32, static_weights=True)
+    b = tl.linear(x, p, s, 0, out_dtype=torch.float32)
+    assert torch.equal(a, b)
+    check(a, oracle_ref(x, p, s, 0), x, s)
+
+
 def test_linear_deterministic():
     x, p, s = layer_inputs(7, 3000, 4096, torch.bfloat16, 128, 4)
     a = tl.linear(x, p, s, 128, out_dtype=torch.float32)
