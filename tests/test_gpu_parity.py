@@ -198,6 +198,44 @@ def test_linear_graph_capture():
     check(out, oracle_ref(x, p, s, 128), x, s)
 
 
+TILE = [
+    # M, N, K, x dtype, group size, out dtype
+    (64, 128, 64, torch.bfloat16, 0, torch.float32),
+    (64, 256, 256, torch.bfloat16, 0, torch.bfloat16),
+    (100, 200, 320, torch.bfloat16, 0, torch.float32),
+    (128, 384, 512, torch.float16, 0, torch.float16),
+    (256, 128, 1024, torch.float16, 128, torch.float32),
+    (300, 300, 768, torch.bfloat16, 128, torch.float32),
+    (70, 130, 384, torch.float16, 128, torch.float16),
+    (512, 256, 2048, torch.bfloat16, 0, torch.float32),
+    (33, 129, 128, torch.bfloat16, 128, torch.bfloat16),
+    (1, 64, 128, torch.float16, 0, torch.float32),
+]
+
+
+@pytest.mark.parametrize("M,N,K,xdt,gs,odt", TILE)
+def test_linear_tile_small(M, N, K, xdt, gs, odt):
+    x, p, s = layer_inputs(M, N, K, xdt, gs, 2, p_reserved=0.01)
+    y = tl.linear(x, p, s, gs, out_dtype=odt, path="tile")
+    torch.cuda.synchronize()
+    check(y, oracle_ref(x, p, s, gs), x, s, what=f"tile {M}x{N}x{K}")
+    assert tl.device_status() == 0
+
+
+@pytest.mark.parametrize("gs", [0, 128])
+def test_linear_tile_every_byte_exact(gs):
+    K = 128
+    p = torch.zeros((256, K // 4), dtype=torch.uint8)
+    p[:, 0] = torch.arange(256, dtype=torch.uint8)
+    x = torch.zeros((64, K), dtype=torch.float32)
+    x[0, :4] = torch.tensor([1.0, 3.0, 9.0, 27.0])
+    x = x.to(torch.float16)
+    s = torch.ones((256,) if gs == 0 else (256, 1), dtype=torch.float16)
+    want = oracle_ref(x, p, s, gs)
+    y = tl.linear(x.to(DEV), p.to(DEV), s.to(DEV), gs, out_dtype=torch.float32, path="tile")
+    assert np.array_equal(y.cpu().double().numpy(), want)
+
+
 # ------------------------------------------------------------------ full-size configs
 def sampled_rows(N, seed, k=48):
     g = np.random.default_rng(seed)
@@ -207,6 +245,7 @@ def sampled_rows(N, seed, k=48):
 
 
 SKINNY_FULL = [(c.key, l, M) for c in CONFIGS.values() for l in c.layers for M in c.Ms if M <= 32]
+TILE_FULL = [(c.key, l, M) for c in CONFIGS.values() for l in c.layers for M in c.Ms if M > 32]
 
 
 @pytest.mark.parametrize("key,layer,M", SKINNY_FULL,
@@ -220,3 +259,17 @@ def test_full_size_skinny_sampled(key, layer, M):
     rows = sampled_rows(layer.N, synth.seed_for(key, layer.name, M) & 0xFFFF)
     ref = oracle_ref(x, p, s, cfg.group_size, rows=rows)
     check(y[:, rows], ref, x, s, rows=rows, what=f"{key} {layer.name} M={M}")
+
+
+@pytest.mark.parametrize("key,layer,M", TILE_FULL,
+                         ids=[f"{k}-{l.name}-M{M}" for k, l, M in TILE_FULL])
+def test_full_size_tile_sampled(key, layer, M):
+    cfg = CONFIGS[key]
+    x, p, s = synth.layer(M, layer.N, layer.K, cfg.x_dtype, cfg.group_size, cfg.s_lo, cfg.s_hi,
+                          (key, layer.name, 0), DEV, cfg.p_reserved)
+    y = tl.linear(x, p, s, cfg.group_size, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    rows = sampled_rows(layer.N, synth.seed_for(key, layer.name, M) & 0xFFFF, k=24)
+    ref = oracle_ref(x, p, s, cfg.group_size, rows=rows)
+    check(y[:, rows], ref, x, s, rows=rows, what=f"{key} {layer.name} M={M}")
+    assert tl.device_status() == 0
