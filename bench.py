@@ -188,42 +188,40 @@ def time_graph(g, stream, steps, warmup, barrier):
 
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(cfg, Ms, budget_s: float, threads: int):
-    """Time the CPU oracle on a bounded sample of the workload: for each
-    projection shape, a slice of output rows at every M.  Returns
-    (packed GB/s of the sample, description)."""
+    """Time the CPU oracle, as it stands, on a bounded sample of the workload:
+    for every distinct (N, K) projection shape and every M, the first R output
+    rows (R = min(N, 256)), cycled until about budget_s seconds of work.
+    Returns (packed-weight GB/s of the sample, description, seconds)."""
     import oracle
     oracle.build()
-    done_bytes, spent = 0, 0.0
-    shapes = {}
+    shapes = []
     for l in cfg.layers:
-        shapes.setdefault((l.N, l.K), l)
-    per_shape = budget_s / max(1, len(shapes) * len(Ms))
-    rows_used = {}
-    for (N, K), l in shapes.items():
+        if (l.N, l.K) not in [(a, b) for a, b, _ in shapes]:
+            shapes.append((l.N, l.K, l.name))
+    name = "f16" if cfg.x_dtype == torch.float16 else "bf16"
+    items = []
+    for N, K, lname in shapes:
+        rows = min(N, 256)
+        p = synth.packed_codes(rows, K, synth.seed_for("cpu", N, K), "cpu").numpy()
+        groups = 0 if cfg.group_size == 0 else K // cfg.group_size
+        s = synth.scales(rows, groups, cfg.s_lo, cfg.s_hi, 1, "cpu")
+        sb = s.view(torch.int16).numpy().view(np.uint16)
         for M in Ms:
             x = synth.activations(M, K, cfg.x_dtype, synth.seed_for("cpu", K, M), "cpu")
             xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
-            name = "f16" if cfg.x_dtype == torch.float16 else "bf16"
-            # calibrate on a small slice, then size the slice to the budget
-            rows = max(threads, 8)
-            while True:
-                p = synth.packed_codes(rows, K, synth.seed_for("cpu", N, K, rows), "cpu").numpy()
-                groups = 0 if cfg.group_size == 0 else K // cfg.group_size
-                s = synth.scales(rows, groups, cfg.s_lo, cfg.s_hi, 1, "cpu")
-                sb = s.view(torch.int16).numpy().view(np.uint16)
-                t0 = time.perf_counter()
-                oracle.linear_from_bits(xb, name, p, sb, cfg.group_size, threads)
-                dt = time.perf_counter() - t0
-                if dt >= 0.2 * per_shape or rows >= N:
-                    break
-                rows = min(N, rows * 4)
-            done_bytes += rows * K // 4
-            spent += dt
-            rows_used[f"{N}x{K}@M{M}"] = rows
-    gbs = done_bytes / spent / 1e9 if spent > 0 else None
-    desc = (f"oracle fp64 C, {threads} threads: per (N,K) shape of {cfg.key} and every M in "
-            f"{list(Ms)}, a slice of output rows {rows_used}; {spent:.1f} s of CPU work; value = "
-            "packed bytes of the slices / CPU time")
+            items.append((xb, p, sb, rows * K // 4, f"{N}x{K}@M{M}[{rows} rows]"))
+    done_bytes, spent, passes = 0, 0.0, 0
+    while spent < budget_s or passes == 0:
+        for xb, p, sb, nbytes, _ in items:
+            t0 = time.perf_counter()
+            oracle.linear_from_bits(xb, name, p, sb, cfg.group_size, threads)
+            spent += time.perf_counter() - t0
+            done_bytes += nbytes
+        passes += 1
+    gbs = done_bytes / spent / 1e9
+    desc = (f"oracle fp64 C with {threads} threads on {len(items)} slices of {cfg.key} "
+            f"({', '.join(i[4] for i in items)}), {passes} passes, {spent:.1f} s of CPU work; "
+            "value = packed bytes of the slices / CPU time")
     return gbs, desc, spent
 
 
@@ -240,10 +238,17 @@ def main():
                     help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--depth", type=int, default=0,
+                    help="override the number of model layers (small cases for profiling)")
+    ap.add_argument("--per-m-reps", type=int, default=0,
+                    help="graph replays for each per-M timing (default: max(20, steps/4))")
     args = ap.parse_args()
 
     rank, world, local = dist_env()
     cfg = CONFIGS[args.workload]
+    if args.depth > 0:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, depth=args.depth)
     Ms = tuple(int(v) for v in args.ms.split(",")) if args.ms else cfg.Ms
     threads = os.cpu_count() or 1
     workload_name = (f"{cfg.key}: {cfg.title}; depth {cfg.depth}; "
@@ -314,12 +319,13 @@ def main():
     calls = stack.calls_per_step()
     pk, pk_src = peaks()
     peak = pk["hbm_gbs"]
-    achieved = ab / (ms_step * 1e-3) / 1e9  # all launches are the skinny kernel here
+    achieved = ab / (ms_step * 1e-3) / 1e9  # every launch of the step is the linear kernel
     per_m = {}
     for M in Ms:  # per-M decode-step time: time one M pass alone
+        reps = args.per_m_reps if args.per_m_reps > 0 else max(20, args.steps // 4)
         gm = capture(lambda M=M: Stack.run_step(_OneM(stack, M), tl), stream)
-        mt, _, _ = time_graph(gm, stream, max(20, args.steps // 4), 3, lambda: None)
-        mt /= max(20, args.steps // 4)
+        mt, _, _ = time_graph(gm, stream, reps, 3, lambda: None)
+        mt /= reps
         per_m[str(M)] = {"us_per_decode_step": round(mt * 1e3, 2),
                          "packed_GBps": round(packed_bytes(cfg) / (mt * 1e-3) / 1e9, 1),
                          "frac_of_hbm": round(algorithmic_bytes(cfg, M) / (mt * 1e-3) / 1e9 / peak, 4),
@@ -376,7 +382,7 @@ def main():
                    "per_M": per_m, "peaks_source": pk_src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "skinny_mma_kernel (every launch of the step)",
+                     "kernel": "ternary_linear kernels (every launch of the step)",
                      "peak_note": f"hbm_gbs of {pk_src} peaks"},
         "cpu_baseline": cpu,
         "e2e": e2e,
