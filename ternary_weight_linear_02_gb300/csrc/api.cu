@@ -48,6 +48,7 @@ int skinny_max_m() {
 //                      =2  no explicit release (dependents start when the grid exits)
 //   TERNARY_SKINNY_SK=n    force the skinny path's K split (cluster size), 0 = automatic
 //   TERNARY_L2_PREFETCH=0  no L2 bulk prefetch before griddepcontrol.wait
+//   TERNARY_SKINNY_CTAS_PER_SM=n  CTAs per SM the tensor-core skinny path aims for (default 2)
 bool pdl_enabled() {
     static const bool v = env_int("TERNARY_PDL", 1) != 0;
     return v;
@@ -59,6 +60,16 @@ int skinny_launch_flags(uint32_t api_flags) {
                             (trig == 2 ? tl::kSkinnyTriggerNever : 0) |
                             (env_int("TERNARY_L2_PREFETCH", 1) ? tl::kSkinnyPrefetchL2 : 0);
     return base | ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kSkinnyStaticWeights : 0);
+}
+
+//   TERNARY_SKINNY_IMPL=mma  use the register-fed mma.sync skinny kernel instead of
+//                            the tcgen05 one
+bool skinny_impl_tc() {
+    static const bool v = [] {
+        const char *e = std::getenv("TERNARY_SKINNY_IMPL");
+        return !(e && e[0] == 'm');
+    }();
+    return v;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -179,6 +190,22 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     }
     if (use == TL_PATH_SKINNY) {
         if (!skinny_ok) return TL_ERR_UNSUPPORTED;
+        if (skinny_impl_tc()) {
+            static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
+            tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
+            if (!tp.ok) return TL_ERR_UNSUPPORTED;
+            tl::SkinnyTcArgs a{};
+            a.x = static_cast<const uint16_t *>(x);
+            a.packed = packed;
+            a.scale = static_cast<const uint16_t *>(scale);
+            a.out = out;
+            a.M = (int)M;
+            a.N = (int)N;
+            a.K = (int)K;
+            a.flags = skinny_launch_flags(flags);
+            a.status = d->status;
+            return from_cuda(tl::launch_skinny_tc(a, bf, group, out_dtype, tp, st, pdl_enabled()));
+        }
         tl::SkinnyArgs a{};
         a.x = static_cast<const uint16_t *>(x);
         a.packed = packed;

@@ -133,11 +133,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 // Bounded wait for phase `parity` of an mbarrier: gives up after ~0.5 s of
 // spinning (a correct program never gets there) and reports false.
+// try_wait that may suspend the thread for up to `ns` nanoseconds while the
+// phase is incomplete (a waiting warp then stops competing for issue slots)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;  // fast path: no clock read
     const long long t0 = clock64();
     for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 255u && clock64() - t0 > (1ll << 30)) return false;
+        if (mbar_try_wait_sleep(bar, parity, 200u)) return true;
+        if ((it & 63u) == 63u && clock64() - t0 > (1ll << 30)) return false;
     }
 }
 // Copy `bytes` (multiple of 16; both addresses 16-byte aligned) from global

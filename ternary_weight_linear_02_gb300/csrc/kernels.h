@@ -60,6 +60,31 @@ SkinnyPlan plan_skinny(int64_t M, int64_t N, int64_t K, int sm_count, int force_
 cudaError_t launch_skinny(const SkinnyArgs &a, bool bf, bool group, int out_dtype,
                           const SkinnyPlan &p, cudaStream_t st, bool pdl);
 
+// ------------------------------------------------------------ skinny path, tensor cores
+struct SkinnyTcArgs {
+    const uint16_t *x;       // [M,K] fp16 or bf16 bits
+    const uint8_t *packed;   // [N,K/4]
+    const uint16_t *scale;   // fp16 [N] or [N,K/128]
+    void *out;               // [M,N]
+    int M, N, K;
+    int kc;                  // k per CTA (multiple of 128), set from the plan
+    int flags;               // kSkinny* bits
+    int *status;             // device status word (bounded-wait failures)
+};
+
+struct SkinnyTcPlan {
+    int nt;         // MMA N (tokens padded to 16 or 32)
+    int row_tiles;  // 128-row blocks
+    int sk;         // K split = cluster size (<= 8)
+    int kc;         // k per CTA
+    bool ok;
+};
+
+SkinnyTcPlan plan_skinny_tc(int64_t M, int64_t N, int64_t K, int sm_count, int force_sk = 0,
+                            int ctas_per_sm = 2);
+cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, bool bf, bool group, int out_dtype,
+                             const SkinnyTcPlan &p, cudaStream_t st, bool pdl);
+
 // ------------------------------------------------------------ tile path
 struct TileArgs {
     const uint16_t *x;       // [M,K]
