@@ -62,14 +62,23 @@ int skinny_launch_flags(uint32_t api_flags) {
     return base | ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kSkinnyStaticWeights : 0);
 }
 
-//   TERNARY_SKINNY_IMPL=mma  use the register-fed mma.sync skinny kernel instead of
-//                            the tcgen05 one
-bool skinny_impl_tc() {
-    static const bool v = [] {
+// Skinny-path kernel choice.  The tcgen05 kernel (decoded weights in TMEM, 128-row
+// tiles, cluster split-K) is faster from M = 3 tokens up; for M <= 2 the register-fed
+// mma.sync kernel (16-row CTAs, no split-K, a much shorter critical path per CTA)
+// measured faster on the 7B-shaped decode set.
+//   TERNARY_SKINNY_IMPL=tc | mma   force one of the two kernels for every M <= 32
+//   TERNARY_SKINNY_TC_MIN_M=n      smallest M sent to the tcgen05 kernel (default 3)
+bool skinny_impl_tc(int64_t M) {
+    static const int mode = [] {
         const char *e = std::getenv("TERNARY_SKINNY_IMPL");
-        return !(e && e[0] == 'm');
+        if (e && e[0] == 'm') return 1;
+        if (e && e[0] == 't') return 2;
+        return 0;
     }();
-    return v;
+    static const int min_m = env_int("TERNARY_SKINNY_TC_MIN_M", 3);
+    if (mode == 1) return false;
+    if (mode == 2) return true;
+    return M >= min_m;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -190,7 +199,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     }
     if (use == TL_PATH_SKINNY) {
         if (!skinny_ok) return TL_ERR_UNSUPPORTED;
-        if (skinny_impl_tc()) {
+        if (skinny_impl_tc(M)) {
             static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
             tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
             if (!tp.ok) return TL_ERR_UNSUPPORTED;

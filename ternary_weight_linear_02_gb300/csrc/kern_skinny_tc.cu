@@ -13,36 +13,40 @@
 //
 // One CTA owns 128 weight rows (one TMEM lane each) x a K range (a multiple of
 // 128).  The K ranges of a row block are the CTAs of one thread-block cluster
-// (split K, <= 8).
-//  * Warp 7: TMA of the packed weights, 128 rows x 128 B (512 k) per stage,
-//    128-byte swizzle, a 4-stage (64 KB) ring.  With static weights the first
-//    stages are requested before griddepcontrol.wait, so a layer's weight
-//    stream starts while the previous kernel is still running.
-//  * Decoder warps 0-3 (thread = weight row = TMEM lane): read 16 B of codes
-//    per 64 k from the staged row (conflict-free thanks to the swizzle),
-//    decode every 2-bit code into 2*t in {+-2, +-0} (exact in fp16 and bf16)
-//    with one shift + one AND per register (tl::pair2: codes j and j+8 of a
-//    16-code word share one f16x2/bf16x2 register) and store each 128-k unit
-//    into a TMEM A stage with tcgen05.st.  Decoders never wait for x.
-//  * Warp 4: TMA of x tiles (NT tokens x 64 k, 128-byte swizzle; token rows
-//    >= M are zero-filled by the TMA unit) into a shared-memory ring.
-//  * Warp 6: permutes each 16-k block of every staged x row in place so that
+// (split K, <= 8).  Two CTAs fit on an SM, so the next layer's CTAs can start
+// (programmatic dependent launch) while this one finishes.
+//  * Warp 8 (producer): TMA of the packed weights, 128 rows x 128 B (512 k) per
+//    stage, 128-byte swizzle, 3-stage ring; with static weights the first
+//    stages are requested before griddepcontrol.wait.  After the wait, one
+//    3-D TMA per 512-k x stage (8 chunks of 64 k x NT token rows; rows >= M
+//    are zero-filled by the TMA unit).
+//  * Warps 0-7 (two decoder sets; thread = weight row = TMEM lane): read 16 B
+//    of codes per 64 k from the staged row (conflict-free thanks to the
+//    swizzle), decode every 2-bit code into 2*t in {+-2, +-0} (exact in fp16
+//    and bf16) with one shift + one AND per register (tl::pair2: codes j and
+//    j+8 of a 16-code word share one f16x2/bf16x2 register) and store each
+//    128-k unit into a TMEM A stage with tcgen05.st.  Set s decodes units
+//    u = s mod 2.  Decoders never wait for x.
+//  * Warp 9: permutes each 16-k block of every staged x row in place so that
 //    MMA k-slot (2j, 2j+1) holds x[j], x[j+8] -- the order in which pair2
 //    packs the weights -- then hands the stage to the MMA.
-//  * Warp 5: TMEM allocation and tcgen05.mma (kind::f16, M = 128 rows,
-//    N = NT tokens, A from TMEM, B from shared memory, fp32 D in TMEM).
-//  * Scales.  Channel: one accumulator over the whole K range, times
-//    0.5*s[n] after the split-K sum.  Group: each 128-k unit accumulates into
-//    its own TMEM slot; the decoder thread that owns the row reads it back
-//    (tcgen05.ld) and folds acc += 0.5*s[n,g] * D_g in fp32 registers.
-//  * Split K: each CTA leaves its fp32 partial [tokens][128 rows] in its own
-//    shared memory; after a cluster barrier CTA r sums the slice of rows it
-//    owns over ranks 0..sk-1 in that fixed order (distributed shared memory
-//    loads), so the result is bit-identical run to run and nothing is
+//  * Warps 10-11 (MMA issuers): issuer s runs the tcgen05.mma (kind::f16,
+//    M = 128 rows, N = NT tokens, A from TMEM, B from shared memory) of units
+//    u = s mod 2 into its own fp32 TMEM accumulator.  One thread can issue a
+//    small-N MMA only every few dozen cycles, hence two issuers.
+//  * Scales.  Channel: the two issuers' accumulators are summed, reduced over
+//    the split K, then multiplied by 0.5*s[n] (the 2 of the +-2 decode).
+//    Group: each 128-k unit lands in its issuer's accumulator slot; the decoder
+//    set that owns the unit reads it back (tcgen05.ld) and folds
+//    acc += 0.5*s[n,g] * D_g in fp32 registers; the two sets' sums are added.
+//  * Split K: every row's fp32 partial is stored into the shared memory of the
+//    cluster CTA that owns the row (st.shared::cluster) and announced with a
+//    remote mbarrier arrive; the owner sums senders 0..sk-1 in that fixed
+//    order, so the result is bit-identical run to run and nothing is
 //    allocated.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status
-// word and the CTA stops issuing work, still joins the cluster barriers, frees
-// its TMEM and returns.
+// word and the CTA stops issuing work, drains its copies and MMAs, still joins
+// the cluster barrier, frees its TMEM and returns.
 #include <cuda.h>
 
 #include "kernels.h"
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t tmem = *tmem_slot;
     const uint32_t dbase = tmem + (uint32_t)(C::NA * 64);
     // dependents may start once every CTA of this grid holds its TMEM
-    pdl_launch_dependents();
+    if (!(a.flags & (kSkinnyTriggerLate | kSkinnyTriggerNever))) pdl_launch_dependents();
 
     auto give_up = [&]() {
         *abort_flag = 1;
@@ -559,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     __syncwarp();
+    if (a.flags & kSkinnyTriggerLate) pdl_launch_dependents();
     if (sk > 1 && warp >= 4) cluster_wait_aligned();  // set 1 and the helper warps
     tc::fence_before_sync();
     __syncthreads();
