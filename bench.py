@@ -33,7 +33,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from ternary_weight_linear_02_gb300 import synth  # noqa: E402
+from ternary_weight_linear_02_gb300 import dist_util, synth  # noqa: E402
 from ternary_weight_linear_02_gb300.workloads import CONFIGS, algorithmic_bytes, flops, packed_bytes  # noqa: E402
 
 METRIC = "packed-weight HBM GB/s and % of roofline per ternary_linear; µs/decode-step"
@@ -242,6 +242,9 @@ def main():
                     help="override the number of model layers (small cases for profiling)")
     ap.add_argument("--per-m-reps", type=int, default=0,
                     help="graph replays for each per-M timing (default: max(20, steps/4))")
+    ap.add_argument("--comparator", action="store_true",
+                    help="also time the same stack with weights dequantised once to bf16 "
+                         "(t * scale) and torch.matmul (cuBLAS)")
     args = ap.parse_args()
 
     rank, world, local = dist_env()
@@ -306,16 +309,11 @@ def main():
     ms_total, t0, t1 = time_graph(g, stream, args.steps, args.warmup, barrier)
     clocks.window(t0, t1)
     clk = clocks.stop()
-    ms_step = ms_total / args.steps
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_step], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_step = float(tt.item())
+    ms_step = dist_util.max_over_ranks(ms_total / args.steps, dev)
 
     pb = packed_bytes(cfg) * len(Ms)
     ab = sum(algorithmic_bytes(cfg, M) for M in Ms)
-    value = world * pb / (ms_step * 1e-3) / 1e9
+    value = dist_util.job_throughput(pb, ms_step, world) / 1e9
     calls = stack.calls_per_step()
     pk, pk_src = peaks()
     peak = pk["hbm_gbs"]
@@ -355,15 +353,14 @@ def main():
 
         ge = capture(e2e_step, stream)
         e_ms, _, _ = time_graph(ge, stream, args.steps, args.warmup, barrier)
-        e_step = e_ms / args.steps
-        if world > 1:
-            import torch.distributed as dist
-            tt = torch.tensor([e_step], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_step = float(tt.item())
-        e2e = {"value": world * pb / (e_step * 1e-3) / 1e9, "unit": "GB/s",
+        e_step = dist_util.max_over_ranks(e_ms / args.steps, dev)
+        e2e = {"value": dist_util.job_throughput(pb, e_step, world) / 1e9, "unit": "GB/s",
                "ms_per_step": e_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
         del ge
+
+    comparator = None
+    if args.comparator:
+        comparator = time_comparator(stack, tl, stream, Ms, args)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -387,6 +384,7 @@ def main():
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": calls * args.steps,
+        "comparator": comparator,
         "clocks": clk,
     }
     if rank == 0:
@@ -395,6 +393,51 @@ def main():
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_comparator(stack, tl, stream, Ms, args):
+    """The same decode stack with each layer's weights dequantised once to bf16
+    (t from ternary_unpack, times the scale) and run with torch.matmul (cuBLAS):
+    the dequantise-at-load route the pages compare against.  Reported as the same
+    packed-weight GB/s (packed bytes of the step / step time) for comparison."""
+    cfg = stack.cfg
+    W = []
+    for d in range(cfg.depth):
+        row = []
+        for j, l in enumerate(cfg.layers):
+            packed, scale = stack.w[d][j]
+            t, _ = tl.unpack(packed)
+            if cfg.group_size == 0:
+                w = t.to(torch.float32) * scale.to(torch.float32)[:, None]
+            else:
+                w = (t.to(torch.float32).view(l.N, -1, cfg.group_size)
+                     * scale.to(torch.float32)[:, :, None]).view(l.N, l.K)
+            row.append(w.to(cfg.x_dtype))
+            del t, w
+        W.append(row)
+    torch.cuda.synchronize()
+    res = {"kind": "weights dequantised once to " + ("bf16" if cfg.x_dtype == torch.bfloat16 else "fp16")
+           + " (t * scale) + torch.matmul (cuBLAS), same stack and inputs", "unit": "GB/s", "per_M": {}}
+    tot_ms = 0.0
+    for M in Ms:
+        def step(M=M):
+            for d in range(cfg.depth):
+                for j in range(len(cfg.layers)):
+                    torch.matmul(stack.x[M][d][j], W[d][j].t(), out=stack.out[M][d][j])
+        step()
+        g = capture(step, stream)
+        reps = args.per_m_reps if args.per_m_reps > 0 else max(20, args.steps // 4)
+        mt, _, _ = time_graph(g, stream, reps, 3, lambda: None)
+        mt /= reps
+        tot_ms += mt
+        res["per_M"][str(M)] = {"us_per_decode_step": round(mt * 1e3, 2),
+                                "packed_GBps": round(packed_bytes(cfg) / (mt * 1e-3) / 1e9, 1),
+                                "bf16_weight_GBps": round(packed_bytes(cfg) * 8 / (mt * 1e-3) / 1e9, 1)}
+        del g
+    res["value"] = packed_bytes(cfg) * len(Ms) / (tot_ms * 1e-3) / 1e9
+    del W
+    torch.cuda.empty_cache()
+    return res
 
 
 class _OneM:

@@ -273,3 +273,23 @@ def test_full_size_tile_sampled(key, layer, M):
     ref = oracle_ref(x, p, s, cfg.group_size, rows=rows)
     check(y[:, rows], ref, x, s, rows=rows, what=f"{key} {layer.name} M={M}")
     assert tl.device_status() == 0
+
+
+# ------------------------------------------------------------------ tensor-parallel shards
+@pytest.mark.parametrize("gs", [0, 128])
+def test_tp_shards_reassemble(gs):
+    """Per-shard calls rebuild the whole layer: a column split (rows of packed and
+    scale cut together) concatenates; a K split's fp32 partials add up."""
+    from ternary_weight_linear_02_gb300 import shard
+    M, N, K = 8, 512, 2048
+    x, p, s = layer_inputs(M, N, K, torch.bfloat16, gs, 7, p_reserved=0.01)
+    ref = oracle_ref(x, p, s, gs)
+    ys = [tl.linear(x, pi, si, gs, out_dtype=torch.float32)
+          for pi, si in shard.split_n(p, s, [128, 256, 128])]
+    check(torch.cat(ys, dim=1), ref, x, s, what="column shards")
+    tot = None
+    for pi, si, k0 in shard.split_k(p, s, shard.even_cuts(K, 4, 128 if gs else 64)):
+        xs = x[:, k0:k0 + pi.shape[1] * 4].contiguous()
+        part = tl.linear(xs, pi, si, gs, out_dtype=torch.float32)
+        tot = part if tot is None else tot + part
+    check(tot, ref, x, s, what="K shards")
