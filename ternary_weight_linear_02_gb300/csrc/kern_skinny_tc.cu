@@ -678,10 +678,11 @@ SkinnyTcPlan plan_skinny_tc(int64_t M, int64_t N, int64_t K, int sm_count, int f
     p.nt = M <= 16 ? 16 : 32;
     p.row_tiles = (int)((N + 127) / 128);
     const int units = (int)((K + 127) / 128);
-    // enough CTAs to cover ctas_per_sm waves of the SMs: K is split (a thread-block
-    // cluster per row block) when there are too few row blocks
+    // K is split (a thread-block cluster per row block) until the CTAs fill the
+    // ctas_per_sm resident slots of every SM -- but never beyond them: a second,
+    // partial wave costs a whole CTA's latency
     const int64_t target = (int64_t)sm_count * (ctas_per_sm > 0 ? ctas_per_sm : 2);
-    int sk = force_sk > 0 ? force_sk : (int)((target + p.row_tiles - 1) / p.row_tiles);
+    int sk = force_sk > 0 ? force_sk : (int)(target / p.row_tiles);
     if (sk < 1) sk = 1;
     if (sk > 8) sk = 8;
     if (sk > units) sk = units;
