@@ -38,8 +38,8 @@ extern "C" {
 typedef enum {
     TL_OK = 0,
     TL_ERR_NULL = 1,        /* a required pointer is NULL                        */
-    TL_ERR_SHAPE = 2,       /* negative size, K % 4 != 0, K % 128 != 0 in group
-                               mode, or a size beyond the supported range        */
+    TL_ERR_SHAPE = 2,       /* negative size, K % 4 != 0, K not a multiple of the
+                               group size, or a size beyond the supported range  */
     TL_ERR_DTYPE = 3,       /* unknown dtype code or unsupported group size      */
     TL_ERR_ALIGN = 4,       /* pointer not 16-byte aligned, or K % 64 != 0 for
                                ternary_linear (packed rows must be 16-byte pitched) */
@@ -93,11 +93,15 @@ tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
  *   group_size == 128 : per-(row, 128-wide K group) scale, scale is fp16 [N, K/128]
  *                       out[m,n] = sum_g scale[n,g] * sum_{k in group g} t[n,k] x[m,k]
  *                       ("三元量化模型接入vLLM…完整实战" §1.1, §3.1, §4.2)
+ *   group_size == 64  : the same with 64-wide groups, scale fp16 [N, K/64]
+ *                       ("Bonsai 2 27B" port §4.2, §5.2); served by the tile
+ *                       kernel for every M (TL_PATH_SKINNY returns
+ *                       TL_ERR_UNSUPPORTED for it)
  *   x_dtype  : TL_F16 or TL_BF16.  scale is always fp16.
  *   out_dtype: TL_F16, TL_BF16 or TL_F32.  Accumulation is fp32; a 16-bit
  *              output is rounded to nearest even from fp32.
- *   Sizes: M, N >= 0; K >= 0 with K % 64 == 0 (and K % 128 == 0 in group
- *   mode).  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *   Sizes: M, N >= 0; K >= 0 with K % 64 == 0 (and K a multiple of the group
+ *   size in group mode).  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
  *   Fused layers (QKV, gate/up) are one call over the stacked rows: shard i
  *   occupies rows [off_i, off_i + N_i) of packed and of scale, and columns
  *   [off_i, off_i + N_i) of out.

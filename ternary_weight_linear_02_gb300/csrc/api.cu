@@ -149,10 +149,10 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
     *noop = false;
     if (x_dtype != TL_F16 && x_dtype != TL_BF16) return TL_ERR_DTYPE;
     if (out_dtype != TL_F16 && out_dtype != TL_BF16 && out_dtype != TL_F32) return TL_ERR_DTYPE;
-    if (group_size != 0 && group_size != 128) return TL_ERR_DTYPE;
+    if (group_size != 0 && group_size != 64 && group_size != 128) return TL_ERR_DTYPE;
     if (M < 0 || N < 0 || K < 0) return TL_ERR_SHAPE;
     if (K % 4 != 0) return TL_ERR_SHAPE;
-    if (group_size == 128 && K % 128 != 0) return TL_ERR_SHAPE;
+    if (group_size > 0 && K % group_size != 0) return TL_ERR_SHAPE;
     const int64_t lim = (int64_t)1 << 30;
     if (M >= lim || N >= lim || K >= lim) return TL_ERR_SHAPE;
     if (M == 0 || N == 0) {
@@ -187,18 +187,21 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)(M * N) * dtype_size(out_dtype), st));
 
     const bool bf = x_dtype == TL_BF16;
-    const bool group = group_size == 128;
+    const bool group = group_size != 0;
+    // 64-wide groups are served by the tile kernel (it applies the scale per
+    // 64-k chunk); the skinny kernels fold scales per 128-k unit
+    const bool g64 = group_size == 64;
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
     tl::SkinnyPlan plan = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
     const bool skinny_ok = plan.ok;
     const bool tile_ok = tl::tile_supported(M, N, K);
     int use = path;
     if (use == TL_PATH_AUTO) {
-        use = (M <= skinny_max_m() && skinny_ok) ? TL_PATH_SKINNY : TL_PATH_TILE;
-        if (use == TL_PATH_TILE && !tile_ok && skinny_ok) use = TL_PATH_SKINNY;
+        use = (M <= skinny_max_m() && skinny_ok && !g64) ? TL_PATH_SKINNY : TL_PATH_TILE;
+        if (use == TL_PATH_TILE && !tile_ok && skinny_ok && !g64) use = TL_PATH_SKINNY;
     }
     if (use == TL_PATH_SKINNY) {
-        if (!skinny_ok) return TL_ERR_UNSUPPORTED;
+        if (!skinny_ok || g64) return TL_ERR_UNSUPPORTED;
         if (skinny_impl_tc(M)) {
             static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
             tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
@@ -236,6 +239,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
+    a.gshift = g64 ? 6 : 7;
     a.status = d->status;
     return from_cuda(tl::launch_tile(a, bf, group, out_dtype, d->sm_count, st, pdl_enabled()));
 }
@@ -329,7 +333,7 @@ const char *ternary_status_string(int32_t status) {
     case TL_OK: return "TL_OK";
     case TL_ERR_NULL: return "TL_ERR_NULL: a required pointer is NULL";
     case TL_ERR_SHAPE: return "TL_ERR_SHAPE: invalid or unsupported sizes";
-    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size or path code";
+    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size (0, 64, 128) or path code";
     case TL_ERR_ALIGN: return "TL_ERR_ALIGN: pointer not 16-byte aligned or K % 64 != 0";
     case TL_ERR_VALUE: return "TL_ERR_VALUE: invalid or reserved values present";
     case TL_ERR_CUDA: return "TL_ERR_CUDA: a CUDA call or kernel launch failed";

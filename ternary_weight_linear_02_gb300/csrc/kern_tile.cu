@@ -3,8 +3,10 @@
 // out[m,n] = sum_k t[n,k] x[m,k] with a per-channel scale (Qwen2.5-7B
 // ternary-in-vLLM write-up, m.nxbn.cn/news/169761, §3.2, §4.2) or a
 // per-128-wide-K-group scale ("三元量化模型接入vLLM：从逆向加载到Kernel优化的完整实战",
-// trdm.cn/news/729035, §3.1, §4.2); codes decoded with the table of that page's
-// §3.1.
+// trdm.cn/news/729035, §3.1, §4.2) -- or 64-wide groups, the variant of the
+// "Bonsai 2 27B" port (m.xxqk.cn/news/593501, §4.2, §5.2); codes decoded with
+// the table of the first page's §3.1.  The scale is applied per 64-k chunk, so
+// either group size is one chunk or two.
 //
 // One CTA computes a 128 (weight rows n) x BN (tokens m) output tile:
 //   D[n, m] = sum_k A[n, k] B[k, m],  A = decoded weights, B = x^T.
@@ -170,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t Kq = a.K >> 2;
         const uint8_t *prow = a.packed + (int64_t)(rowok ? n : 0) * Kq;
         const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-        const int ngk = a.K >> 7;
+        const int ngk = a.K >> a.gshift;  // scale groups per row (G = 64 or 128)
         const uint16_t *srow = a.scale + (SMODE == kChannel ? 0 : (int64_t)(rowok ? n : 0) * ngk);
 
         uint4 cur = rowok && nchunks > 0 ? *reinterpret_cast<const uint4 *>(prow) : make_uint4(0, 0, 0, 0);
@@ -190,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_word_adjacent(codes.w, r + 24);
             uint32_t rl[32];
             if constexpr (SMODE != kChannel) {
-                const uint16_t sbits = rowok ? srow[(c * kKC) >> 7] : (uint16_t)0;
+                const uint16_t sbits = rowok ? srow[(c * kKC) >> a.gshift] : (uint16_t)0;
                 const float sf = h2f(sbits);
                 if constexpr (SMODE == kFold) {
                     // fp16: (+-2) * (s/2) = +-s exactly

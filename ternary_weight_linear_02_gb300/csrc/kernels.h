@@ -89,9 +89,10 @@ cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, bool bf, bool group, int out
 struct TileArgs {
     const uint16_t *x;       // [M,K]
     const uint8_t *packed;   // [N,K/4]
-    const uint16_t *scale;   // fp16 [N] or [N,K/128]
+    const uint16_t *scale;   // fp16 [N] or [N,K/G]
     void *out;               // [M,N]
     int M, N, K;
+    int gshift;              // log2 of the group size G (6 or 7) in group mode
     int *status;             // device status word (bounded-wait failures)
 };
 

@@ -293,3 +293,31 @@ def test_tp_shards_reassemble(gs):
         part = tl.linear(xs, pi, si, gs, out_dtype=torch.float32)
         tot = part if tot is None else tot + part
     check(tot, ref, x, s, what="K shards")
+
+
+# ------------------------------------------------------------------ 64-wide scale groups
+G64 = [
+    # M, N, K, x dtype, out dtype
+    (1, 200, 512, torch.bfloat16, torch.float32),
+    (4, 129, 1088, torch.float16, torch.float32),
+    (16, 300, 4096, torch.bfloat16, torch.bfloat16),
+    (33, 256, 640, torch.float16, torch.float16),
+    (300, 384, 2048, torch.bfloat16, torch.float32),
+]
+
+
+@pytest.mark.parametrize("M,N,K,xdt,odt", G64)
+def test_linear_group64(M, N, K, xdt, odt):
+    x, p, s = layer_inputs(M, N, K, xdt, 64, 3, p_reserved=0.01)
+    assert s.shape == (N, K // 64)
+    y = tl.linear(x, p, s, 64, out_dtype=odt)
+    torch.cuda.synchronize()
+    check(y, oracle_ref(x, p, s, 64), x, s, what=f"g64 {M}x{N}x{K}")
+    assert tl.device_status() == 0
+
+
+def test_group64_skinny_path_refused():
+    x, p, s = layer_inputs(2, 64, 256, torch.bfloat16, 64, 4)
+    with pytest.raises(tl.TernaryError) as e:
+        tl.linear(x, p, s, 64, path="skinny")
+    assert e.value.status == 8  # TL_ERR_UNSUPPORTED
