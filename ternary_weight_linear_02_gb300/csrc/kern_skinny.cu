@@ -1,4 +1,9 @@
-// kern_skinny.cu -- decode-shaped ternary linear (M <= 32 tokens).
+// kern_skinny.cu -- decode-shaped ternary linear on register-fed warp MMAs.
+//
+// Serves M <= 2 tokens by default (the tcgen05 kernel in kern_skinny_tc.cu
+// takes M >= 3): its 16-row CTAs need no split K for most layers, which keeps
+// each CTA's critical path short -- the quantity that decides the time of a
+// single-token decode layer.  It can serve any M <= 32 when forced.
 //
 // out[m,n] = sum_k t[n,k] x[m,k], scaled per output channel
 // (Qwen2.5-7B ternary-in-vLLM write-up, m.nxbn.cn/news/169761, §3.2, §4.2) or
