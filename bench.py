@@ -131,15 +131,25 @@ class Stack:
                                      synth.seed_for(cfg.key, d, l.name, "s"), dev)
                 row.append((packed, scale))
             self.w.append(row)
-        self.x, self.out = {}, {}
+        # per M: every call's x and out are slices of one flat buffer, so an
+        # end-to-end step moves all of a pass's inputs / outputs in one copy each
+        self.x, self.out, self.xflat, self.oflat = {}, {}, {}, {}
         for M in Ms:
-            xs, outs = [], []
+            nx = sum(M * l.K for l in cfg.layers) * cfg.depth
+            no = sum(M * l.N for l in cfg.layers) * cfg.depth
+            self.xflat[M] = torch.empty(nx, dtype=cfg.x_dtype, device=dev)
+            self.oflat[M] = torch.empty(no, dtype=cfg.x_dtype, device=dev)
+            xs, outs, ox, oo = [], [], 0, 0
             for d in range(cfg.depth):
                 xr, orow = [], []
                 for l in cfg.layers:
-                    xr.append(synth.activations(M, l.K, cfg.x_dtype,
-                                                synth.seed_for(cfg.key, d, l.name, "x", M), dev))
-                    orow.append(torch.empty((M, l.N), dtype=cfg.x_dtype, device=dev))
+                    xv = self.xflat[M][ox:ox + M * l.K].view(M, l.K)
+                    xv.copy_(synth.activations(M, l.K, cfg.x_dtype,
+                                               synth.seed_for(cfg.key, d, l.name, "x", M), dev))
+                    xr.append(xv)
+                    orow.append(self.oflat[M][oo:oo + M * l.N].view(M, l.N))
+                    ox += M * l.K
+                    oo += M * l.N
                 xs.append(xr)
                 outs.append(orow)
             self.x[M], self.out[M] = xs, outs
@@ -331,25 +341,20 @@ def main():
         del gm
 
     # end to end: pinned host x -> device, the calls, device out -> pinned host
+    # (one copy per M pass in each direction: every call's x / out is a slice)
     e2e = None
     if not args.no_e2e:
-        hx = {M: [[stack.x[M][d][j].cpu().pin_memory() for j in range(len(cfg.layers))]
-                  for d in range(cfg.depth)] for M in Ms}
-        ho = {M: [[torch.empty(stack.out[M][d][j].shape, dtype=cfg.x_dtype).pin_memory()
-                   for j in range(len(cfg.layers))] for d in range(cfg.depth)] for M in Ms}
-        h2d = sum(t.numel() * t.element_size() for M in Ms for r in hx[M] for t in r)
-        d2h = sum(t.numel() * t.element_size() for M in Ms for r in ho[M] for t in r)
+        hx = {M: stack.xflat[M].cpu().pin_memory() for M in Ms}
+        ho = {M: torch.empty(stack.oflat[M].shape, dtype=cfg.x_dtype).pin_memory() for M in Ms}
+        h2d = sum(t.numel() * t.element_size() for t in hx.values())
+        d2h = sum(t.numel() * t.element_size() for t in ho.values())
 
         def e2e_step():
             for M in Ms:
-                for d in range(cfg.depth):
-                    for j in range(len(cfg.layers)):
-                        stack.x[M][d][j].copy_(hx[M][d][j], non_blocking=True)
+                stack.xflat[M].copy_(hx[M], non_blocking=True)
             stack.run_step(tl)
             for M in Ms:
-                for d in range(cfg.depth):
-                    for j in range(len(cfg.layers)):
-                        ho[M][d][j].copy_(stack.out[M][d][j], non_blocking=True)
+                ho[M].copy_(stack.oflat[M], non_blocking=True)
 
         ge = capture(e2e_step, stream)
         e_ms, _, _ = time_graph(ge, stream, args.steps, args.warmup, barrier)
