@@ -367,6 +367,13 @@ def main():
     if args.comparator:
         comparator = time_comparator(stack, tl, stream, Ms, args)
 
+    # a kernel wait that gave up (bounded waits) leaves a non-zero status word:
+    # the outputs of that call are not valid, so the line says so
+    torch.cuda.synchronize()
+    dev_status = tl.device_status(clear=True)
+    if dev_status != 0:
+        print(f"bench: device status {tl.status_string(dev_status)} after the timed runs", file=sys.stderr)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, desc, _ = oracle_sample(cfg, Ms, args.cpu_budget, threads)
@@ -391,6 +398,7 @@ def main():
         "gpu_launches": calls * args.steps,
         "comparator": comparator,
         "clocks": clk,
+        "device_status": tl.status_string(dev_status),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

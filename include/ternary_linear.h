@@ -97,6 +97,10 @@ tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
  *                       ("Bonsai 2 27B" port §4.2, §5.2); served by the tile
  *                       kernel for every M (TL_PATH_SKINNY returns
  *                       TL_ERR_UNSUPPORTED for it)
+ *   group_size == 256 : the same with 256-wide groups, scale fp16 [N, K/256]
+ *                       (the coarser per-group choice of "第13章 量化：精度与速度的
+ *                       工程平衡" §13.3.3); every path serves it
+ *   Any other group_size returns TL_ERR_DTYPE.
  *   x_dtype  : TL_F16 or TL_BF16.  scale is always fp16.
  *   out_dtype: TL_F16, TL_BF16 or TL_F32.  Accumulation is fp32; a 16-bit
  *              output is rounded to nearest even from fp32.

@@ -149,7 +149,8 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
     *noop = false;
     if (x_dtype != TL_F16 && x_dtype != TL_BF16) return TL_ERR_DTYPE;
     if (out_dtype != TL_F16 && out_dtype != TL_BF16 && out_dtype != TL_F32) return TL_ERR_DTYPE;
-    if (group_size != 0 && group_size != 64 && group_size != 128) return TL_ERR_DTYPE;
+    if (group_size != 0 && group_size != 64 && group_size != 128 && group_size != 256)
+        return TL_ERR_DTYPE;
     if (M < 0 || N < 0 || K < 0) return TL_ERR_SHAPE;
     if (K % 4 != 0) return TL_ERR_SHAPE;
     if (group_size > 0 && K % group_size != 0) return TL_ERR_SHAPE;
@@ -191,6 +192,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     // 64-wide groups are served by the tile kernel (it applies the scale per
     // 64-k chunk); the skinny kernels fold scales per 128-k unit
     const bool g64 = group_size == 64;
+    const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
     tl::SkinnyPlan plan = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
     const bool skinny_ok = plan.ok;
@@ -214,6 +216,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
             a.M = (int)M;
             a.N = (int)N;
             a.K = (int)K;
+            a.gshift = gshift;
             a.flags = skinny_launch_flags(flags);
             a.status = d->status;
             return from_cuda(tl::launch_skinny_tc(a, bf, group, out_dtype, tp, st, pdl_enabled()));
@@ -226,6 +229,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
         a.M = (int)M;
         a.N = (int)N;
         a.K = (int)K;
+        a.gshift = gshift;
         a.flags = skinny_launch_flags(flags);
         a.status = d->status;
         return from_cuda(tl::launch_skinny(a, bf, group, out_dtype, plan, st, pdl_enabled()));
@@ -239,7 +243,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     a.M = (int)M;
     a.N = (int)N;
     a.K = (int)K;
-    a.gshift = g64 ? 6 : 7;
+    a.gshift = gshift;
     a.status = d->status;
     return from_cuda(tl::launch_tile(a, bf, group, out_dtype, d->sm_count, st, pdl_enabled()));
 }

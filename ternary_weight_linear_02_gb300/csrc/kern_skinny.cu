@@ -220,15 +220,17 @@ __global__ void __launch_bounds__(32 * kNW) skinny_mma_kernel(SkinnyArgs a) {
     const int row_g = tile * 16 + g;
     const uint8_t *cg0 = codes + (size_t)row_g * a.row_stride + 8 * t;
     const uint8_t *cg8 = cg0 + (size_t)8 * a.row_stride;
-    const int ngk = a.K >> 7;  // scale groups per row (group mode)
+    const int ngk = a.K >> a.gshift;  // scale groups per row (group mode, G = 128 or 256)
     const bool ok0 = n0 + row_g < a.N, ok8 = n0 + row_g + 8 < a.N;
-    const uint16_t *s0 = a.scale + (GROUP ? (int64_t)(ok0 ? n0 + row_g : 0) * ngk + (kb >> 7) : 0);
-    const uint16_t *s8 = a.scale + (GROUP ? (int64_t)(ok8 ? n0 + row_g + 8 : 0) * ngk + (kb >> 7) : 0);
+    const uint16_t *s0 = a.scale + (GROUP ? (int64_t)(ok0 ? n0 + row_g : 0) * ngk : 0);
+    const uint16_t *s8 = a.scale + (GROUP ? (int64_t)(ok8 ? n0 + row_g + 8 : 0) * ngk : 0);
+    // 128-k group grp of this warp's range belongs to scale group ((kb >> 7) + grp) >> gsh
+    const int g0 = kb >> 7, gsh = a.gshift - 7;
 
     uint16_t sn0 = 0, sn8 = 0;  // next group's scales (group mode)
     if (GROUP && gb < ge) {
-        sn0 = ok0 ? s0[gb] : (uint16_t)0;
-        sn8 = ok8 ? s8[gb] : (uint16_t)0;
+        sn0 = ok0 ? s0[(g0 + gb) >> gsh] : (uint16_t)0;
+        sn8 = ok8 ? s8[(g0 + gb) >> gsh] : (uint16_t)0;
     }
     for (int grp = ok ? gb : ge; grp < ge; ++grp) {
         const uint2 w0 = *reinterpret_cast<const uint2 *>(cg0 + grp * 32);
@@ -238,8 +240,8 @@ __global__ void __launch_bounds__(32 * kNW) skinny_mma_kernel(SkinnyArgs a) {
             sc0 = h2f(sn0);
             sc8 = h2f(sn8);
             if (grp + 1 < ge) {
-                sn0 = ok0 ? s0[grp + 1] : (uint16_t)0;
-                sn8 = ok8 ? s8[grp + 1] : (uint16_t)0;
+                sn0 = ok0 ? s0[(g0 + grp + 1) >> gsh] : (uint16_t)0;
+                sn8 = ok8 ? s8[(g0 + grp + 1) >> gsh] : (uint16_t)0;
             }
 #pragma unroll
             for (int c = 0; c < NC; ++c)

@@ -405,8 +405,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int row = q * 32 + lane;
         const int n = n0 + row;
         const bool rowok = n < a.N;
-        const uint16_t *srow =
-            GROUP ? a.scale + (int64_t)(rowok ? n : 0) * (a.K >> 7) + (k0 >> 7) : a.scale;
+        // group mode: unit v (128 k) of this CTA uses scale group ((k0 >> 7) + v) >> (gshift - 7)
+        const uint16_t *srow = GROUP ? a.scale + (int64_t)(rowok ? n : 0) * (a.K >> a.gshift) : a.scale;
+        const int g0 = k0 >> 7, gsh = a.gshift - 7;
         const uint32_t tlane = tmem + ((uint32_t)(q * 32) << 16);
         const uint8_t *wrow = wring + row * 128;
         const int sw = row & 7;  // 128-byte swizzle of this staged row
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             c0 = *reinterpret_cast<const uint4 *>(stage + (((2 * uw) ^ sw) << 4));
             c1 = (2 * v + 1 < nch) ? *reinterpret_cast<const uint4 *>(stage + (((2 * uw + 1) ^ sw) << 4))
                                    : make_uint4(0, 0, 0, 0);
-            su = (GROUP && rowok) ? 0.5f * h2f(srow[v]) : 0.f;
+            su = (GROUP && rowok) ? 0.5f * h2f(srow[(g0 + v) >> gsh]) : 0.f;
             if (uw >= 2 && w + 1 < nws) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&wempty[ws]);  // codes are in registers

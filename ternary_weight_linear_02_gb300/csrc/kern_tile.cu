@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t Kq = a.K >> 2;
         const uint8_t *prow = a.packed + (int64_t)(rowok ? n : 0) * Kq;
         const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-        const int ngk = a.K >> a.gshift;  // scale groups per row (G = 64 or 128)
+        const int ngk = a.K >> a.gshift;  // scale groups per row (G = 64, 128 or 256)
         const uint16_t *srow = a.scale + (SMODE == kChannel ? 0 : (int64_t)(rowok ? n : 0) * ngk);
 
         uint4 cur = rowok && nchunks > 0 ? *reinterpret_cast<const uint4 *>(prow) : make_uint4(0, 0, 0, 0);

@@ -29,9 +29,10 @@ constexpr int kSkinnyTriggerNever = 8;   // no explicit trigger (dependents star
 struct SkinnyArgs {
     const uint16_t *x;       // [M,K] fp16 or bf16 bits
     const uint8_t *packed;   // [N,K/4]
-    const uint16_t *scale;   // fp16 [N] or [N,K/128]
+    const uint16_t *scale;   // fp16 [N] or [N,K/G]
     void *out;               // [M,N]
     int M, N, K;
+    int gshift;              // log2 of the group size G (7 or 8) in group mode
     int kc;                  // k per CTA (multiple of 128), set from the plan
     int row_stride;          // shared-memory bytes per staged packed row
     int x_off;               // byte offsets in shared memory: staged x fragments,
@@ -64,9 +65,10 @@ cudaError_t launch_skinny(const SkinnyArgs &a, bool bf, bool group, int out_dtyp
 struct SkinnyTcArgs {
     const uint16_t *x;       // [M,K] fp16 or bf16 bits
     const uint8_t *packed;   // [N,K/4]
-    const uint16_t *scale;   // fp16 [N] or [N,K/128]
+    const uint16_t *scale;   // fp16 [N] or [N,K/G]
     void *out;               // [M,N]
     int M, N, K;
+    int gshift;              // log2 of the group size G (7 or 8) in group mode
     int kc;                  // k per CTA (multiple of 128), set from the plan
     int flags;               // kSkinny* bits
     int *status;             // device status word (bounded-wait failures)

@@ -77,8 +77,8 @@ def test_linear_argument_errors(lib):
     assert lin(lib, xdt=2) == TL_ERR_DTYPE          # fp32 x not supported
     assert lin(lib, xdt=-1) == TL_ERR_DTYPE
     assert lin(lib, odt=5) == TL_ERR_DTYPE
-    assert lin(lib, gs=32) == TL_ERR_DTYPE          # group sizes: 0, 64, 128
-    assert lin(lib, gs=256) == TL_ERR_DTYPE
+    assert lin(lib, gs=32) == TL_ERR_DTYPE          # group sizes: 0, 64, 128, 256
+    assert lin(lib, gs=512) == TL_ERR_DTYPE
     assert lin(lib, path=7) == TL_ERR_DTYPE
     assert lin(lib, flags=2) == TL_ERR_DTYPE
     assert lin(lib, M=-1) == TL_ERR_SHAPE
@@ -86,6 +86,7 @@ def test_linear_argument_errors(lib):
     assert lin(lib, K=130) == TL_ERR_SHAPE           # K % 4
     assert lin(lib, gs=128, K=192) == TL_ERR_SHAPE   # K % 128 in group mode
     assert lin(lib, gs=64, K=96) == TL_ERR_SHAPE     # K % 64 in 64-wide group mode
+    assert lin(lib, gs=256, K=384) == TL_ERR_SHAPE   # K % 256 in 256-wide group mode
     assert lin(lib, M=1 << 31) == TL_ERR_SHAPE
     assert lin(lib, K=96) == TL_ERR_ALIGN             # K % 64
     assert lin(lib, out=0) == TL_ERR_NULL

@@ -316,6 +316,30 @@ def test_linear_group64(M, N, K, xdt, odt):
     assert tl.device_status() == 0
 
 
+# ------------------------------------------------------------------ 256-wide scale groups
+G256 = [
+    # M, N, K, x dtype, out dtype: mma.sync skinny (M <= 2), tcgen05 skinny (3..32),
+    # tile (> 32); K = 2816 = 11 groups, so split-K ranges of 384 k end mid-group
+    (1, 300, 2816, torch.bfloat16, torch.float32),
+    (2, 4096, 2816, torch.float16, torch.float32),
+    (4, 4096, 2816, torch.bfloat16, torch.float32),
+    (16, 129, 1024, torch.float16, torch.bfloat16),
+    (32, 256, 4096, torch.bfloat16, torch.float32),
+    (33, 256, 768, torch.float16, torch.float16),
+    (300, 384, 2048, torch.bfloat16, torch.float32),
+]
+
+
+@pytest.mark.parametrize("M,N,K,xdt,odt", G256)
+def test_linear_group256(M, N, K, xdt, odt):
+    x, p, s = layer_inputs(M, N, K, xdt, 256, 5, p_reserved=0.01)
+    assert s.shape == (N, K // 256)
+    y = tl.linear(x, p, s, 256, out_dtype=odt)
+    torch.cuda.synchronize()
+    check(y, oracle_ref(x, p, s, 256), x, s, what=f"g256 {M}x{N}x{K}")
+    assert tl.device_status() == 0
+
+
 def test_group64_skinny_path_refused():
     x, p, s = layer_inputs(2, 64, 256, torch.bfloat16, 64, 4)
     with pytest.raises(tl.TernaryError) as e:

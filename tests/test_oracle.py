@@ -189,21 +189,22 @@ def test_one_hot_weight_picks_one_input(oracle_mod):
             assert np.array_equal(y[:, 0], sign * 1.5 * x[:, k])
 
 
-def test_group_isolation(oracle_mod):
+@pytest.mark.parametrize("G", [128, 256])
+def test_group_isolation(oracle_mod, G):
     rng = np.random.default_rng(5)
     M, K, N = 2, 512, 3
     x = rng.standard_normal((M, K))
     packed = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
     t = second_formulation(packed)
-    for g in range(K // 128):
-        s = np.zeros((N, K // 128))
+    for g in range(K // G):
+        s = np.zeros((N, K // G))
         s[:, g] = 1.0
-        y = oracle_mod.linear_f64(x, packed, s, 128)
-        want = x[:, g * 128:(g + 1) * 128] @ t[:, g * 128:(g + 1) * 128].T.astype(np.float64)
+        y = oracle_mod.linear_f64(x, packed, s, G)
+        want = x[:, g * G:(g + 1) * G] @ t[:, g * G:(g + 1) * G].T.astype(np.float64)
         np.testing.assert_allclose(y, want, rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("group_size", [0, 128, 64])
+@pytest.mark.parametrize("group_size", [0, 128, 64, 256])
 def test_matches_library_matmul(oracle_mod, group_size):
     """The oracle equals numpy's fp64 matmul of x and the dequantised weight
     (t * s broadcast per row / per group) to rounding."""
