@@ -134,6 +134,27 @@ tl_status ternary_linear_ex(const void *x, int32_t x_dtype, const uint8_t *packe
                             int32_t out_dtype, int64_t M, int64_t N, int64_t K,
                             int32_t path, uint32_t flags, void *stream);
 
+/*
+ * ternary_linear_silu_mul -- a fused gate/up layer followed by the SiLU-gated
+ * product that feeds the down projection:
+ *   g = ternary_linear over rows [0, N)  of packed / scale  (gate shard)
+ *   u = ternary_linear over rows [N, 2N) of packed / scale  (up shard)
+ *   out[m, j] = silu(g[m, j]) * u[m, j],  silu(v) = v / (1 + exp(-v)),  j < N
+ * The stacked layout is the fused gate/up layer of ternary_linear (shards at
+ * row offsets 0 and N; "三元量化模型接入vLLM…完整实战" §3.2).
+ *   packed: [2N, K/4]; scale: fp16 [2N] (group_size 0) or [2N, K/G] (G = 128
+ *   or 256); out: [M, N] in out_dtype; g and u are fp32 (scaled) and the
+ *   product is computed in fp32, then rounded to out_dtype.
+ *   flags: TL_FLAG_STATIC_WEIGHTS or 0.
+ * Served by the decode kernel: M > 32 or group_size 64 return
+ * TL_ERR_UNSUPPORTED; other argument errors as ternary_linear (with 2N rows).
+ * N == 0 or M == 0 is a no-op; K == 0 writes zeros.  Asynchronous on stream.
+ */
+tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed,
+                                  const void *scale, int32_t group_size, void *out,
+                                  int32_t out_dtype, int64_t M, int64_t N, int64_t K,
+                                  uint32_t flags, void *stream);
+
 /* Largest M the automatic dispatch sends to the skinny path (default 32,
  * overridable with the environment variable TERNARY_SKINNY_MAX_M, read once). */
 int32_t ternary_skinny_max_m(void);

@@ -31,7 +31,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-shared", "-fPIC", "-pthread",
-                               "-o", tmp, _SRC])
+                               "-o", tmp, _SRC, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -50,6 +50,8 @@ def _load():
         lib.oracle_pack.restype = i64
         lib.oracle_linear_f64.argtypes = [p, p, p, i64, p, i64, i64, i64, ctypes.c_int]
         lib.oracle_linear_f64.restype = ctypes.c_int
+        lib.oracle_silu_mul_f64.argtypes = [p, p, p, i64, p, i64, i64, i64, ctypes.c_int]
+        lib.oracle_silu_mul_f64.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -135,3 +137,32 @@ def linear_from_bits(x_bits: np.ndarray, x_dtype: str, packed: np.ndarray,
     """Same as linear_f64, taking x and the fp16 scale as raw 16-bit patterns."""
     return linear_f64(bits_to_f64(x_bits, x_dtype), packed, f16_bits_to_f64(scale_bits),
                       group_size, nthreads)
+
+
+def silu_mul_f64(x: np.ndarray, packed: np.ndarray, scale: np.ndarray, group_size: int,
+                 nthreads: int = 1) -> np.ndarray:
+    """h[M,N] = silu(g) * u for a stacked gate/up layer (packed [2N, K/4], scale
+    [2N] or [2N, K/G]; gate rows first), in fp64."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    scale = np.ascontiguousarray(scale, dtype=np.float64)
+    M, K = x.shape
+    N2 = packed.shape[0]
+    if N2 % 2 or packed.shape[1] * 4 != K:
+        raise ValueError("packed must be [2N, K/4]")
+    want = (N2,) if group_size == 0 else (N2, K // group_size)
+    if scale.shape != want:
+        raise ValueError(f"scale shape {scale.shape} != {want}")
+    h = np.empty((M, N2 // 2), dtype=np.float64)
+    rc = _load().oracle_silu_mul_f64(_ptr(x), _ptr(packed), _ptr(scale), int(group_size),
+                                     _ptr(h), M, N2 // 2, K, int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle_silu_mul_f64 rejected its arguments")
+    return h
+
+
+def silu_mul_from_bits(x_bits: np.ndarray, x_dtype: str, packed: np.ndarray,
+                       scale_bits: np.ndarray, group_size: int, nthreads: int = 1) -> np.ndarray:
+    """Same as silu_mul_f64, taking x and the fp16 scale as raw 16-bit patterns."""
+    return silu_mul_f64(bits_to_f64(x_bits, x_dtype), packed, f16_bits_to_f64(scale_bits),
+                        group_size, nthreads)

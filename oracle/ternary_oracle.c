@@ -33,6 +33,7 @@
  * threads.  Every y[m,n] is still computed by one thread in the order written
  * below; threads only decide which n each of them takes.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -187,4 +188,34 @@ int oracle_linear_f64(const double *x, const uint8_t *packed, const double *scal
     free(jobs);
     free(tid);
     return 0;
+}
+
+/*
+ * Gated product of a stacked gate/up layer: the pages quantise the gate, up
+ * and down projections of a Qwen2.5-7B-architecture MLP ("三元量化模型接入vLLM：
+ * 从逆向加载到Kernel优化的完整实战" §1.1, §1.3) but do not write out its
+ * activation; that architecture's MLP feeds down_proj with silu(gate) * up,
+ * silu(v) = v / (1 + exp(-v)).
+ *   packed / scale hold 2N rows: gate rows [0, N), then up rows [N, 2N);
+ *   h[m, j] = silu(g[m, j]) * u[m, j] with g, u the fp64 results of
+ *   oracle_linear_f64 over those rows.  h is [M, N].  Returns 0, or -1 on bad
+ *   arguments (as oracle_linear_f64) or when memory runs out.
+ */
+int oracle_silu_mul_f64(const double *x, const uint8_t *packed, const double *scale,
+                        int64_t group_size, double *h, int64_t M, int64_t N, int64_t K,
+                        int nthreads)
+{
+    if (M < 0 || N < 0) return -1;
+    double *y = (double *)malloc((size_t)(M * 2 * N > 0 ? M * 2 * N : 1) * sizeof(double));
+    if (!y) return -1;
+    int rc = oracle_linear_f64(x, packed, scale, group_size, y, M, 2 * N, K, nthreads);
+    if (rc == 0) {
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t j = 0; j < N; ++j) {
+                const double g = y[m * 2 * N + j], u = y[m * 2 * N + N + j];
+                h[m * N + j] = g / (1.0 + exp(-g)) * u;
+            }
+    }
+    free(y);
+    return rc;
 }

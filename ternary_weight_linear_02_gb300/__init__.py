@@ -19,6 +19,7 @@ import torch
 
 __all__ = [
     "TernaryError", "build", "library_path", "load", "pack", "unpack", "linear", "linear_fused",
+    "linear_silu_mul",
     "device_status", "status_string", "skinny_max_m", "PATHS",
 ]
 
@@ -64,7 +65,10 @@ def load():
     lib.ternary_linear.argtypes = [p, i32, p, p, i32, p, i32, i64, i64, i64, p]
     lib.ternary_linear_ex.argtypes = [p, i32, p, p, i32, p, i32, i64, i64, i64, i32,
                                       ctypes.c_uint32, p]
-    for f in (lib.ternary_pack, lib.ternary_unpack, lib.ternary_linear, lib.ternary_linear_ex):
+    lib.ternary_linear_silu_mul.argtypes = [p, i32, p, p, i32, p, i32, i64, i64, i64,
+                                            ctypes.c_uint32, p]
+    for f in (lib.ternary_pack, lib.ternary_unpack, lib.ternary_linear, lib.ternary_linear_ex,
+              lib.ternary_linear_silu_mul):
         f.restype = ctypes.c_int
     lib.ternary_device_status.argtypes = [ctypes.POINTER(ctypes.c_int32), i32]
     lib.ternary_device_status.restype = ctypes.c_int
@@ -206,3 +210,50 @@ def device_status(clear: bool = True) -> int:
     code = ctypes.c_int32(0)
     _check(load().ternary_device_status(ctypes.byref(code), int(clear)), "ternary_device_status")
     return int(code.value)
+
+
+def linear_silu_mul(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
+                    group_size: int | None = None, out_dtype: torch.dtype | None = None,
+                    out: torch.Tensor | None = None,
+                    static_weights: bool = False) -> torch.Tensor:
+    """silu(g) * u for a fused gate/up layer, in one kernel.
+
+    ``packed`` [2N, K/4] and ``scale`` ([2N] or [2N, K/G]) stack the gate rows
+    then the up rows; g = x @ gate^T, u = x @ up^T; returns [..., N].  Decode
+    shapes only (M <= 32 tokens after flattening the leading dimensions).
+    """
+    _need_cuda(x, packed, scale, out)
+    if x.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("x must be fp16 or bf16")
+    if scale.dtype != torch.float16:
+        raise ValueError("scale must be fp16")
+    if packed.dtype != torch.uint8 or packed.dim() != 2 or packed.shape[0] % 2:
+        raise ValueError("packed must be a 2-D uint8 tensor [2N, K/4]")
+    K = x.shape[-1]
+    lead = x.shape[:-1]
+    M = 1
+    for d in lead:
+        M *= int(d)
+    x2 = x.reshape(M, K).contiguous()
+    N2 = packed.shape[0]
+    N = N2 // 2
+    if packed.shape[1] * 4 != K:
+        raise ValueError(f"packed is [2N, {packed.shape[1]}] but K/4 = {K / 4}")
+    if group_size is None:
+        group_size = 0 if scale.dim() == 1 else K // max(scale.shape[-1], 1)
+    want = (N2,) if group_size == 0 else (N2, K // group_size if group_size else 0)
+    if tuple(scale.shape) != want:
+        raise ValueError(f"scale shape {tuple(scale.shape)} != {want}")
+    odt = out_dtype or x.dtype
+    if out is None:
+        out = torch.empty((M, N), dtype=odt, device=x.device)
+    elif out.shape != (M, N) or not out.is_contiguous() or out.dtype != odt:
+        raise ValueError("out must be a contiguous [M, N] tensor of out_dtype")
+    packed = packed.contiguous()
+    scale = scale.contiguous()
+    rc = load().ternary_linear_silu_mul(_ptr(x2), _DT[x.dtype], _ptr(packed), _ptr(scale),
+                                        int(group_size), _ptr(out), _DT[odt], M, N, K,
+                                        FLAG_STATIC_WEIGHTS if static_weights else 0,
+                                        _stream(x.device))
+    _check(rc, "ternary_linear_silu_mul")
+    return out.reshape(*lead, N)

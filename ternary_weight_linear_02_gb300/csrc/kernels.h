@@ -69,6 +69,7 @@ struct SkinnyTcArgs {
     void *out;               // [M,N]
     int M, N, K;
     int gshift;              // log2 of the group size G (7 or 8) in group mode
+    int nh;                  // SiLU-gated call: gate rows [0, nh), up rows [nh, 2 nh), out [M, nh]
     int kc;                  // k per CTA (multiple of 128), set from the plan
     int flags;               // kSkinny* bits
     int *status;             // device status word (bounded-wait failures)
@@ -86,6 +87,10 @@ SkinnyTcPlan plan_skinny_tc(int64_t M, int64_t N, int64_t K, int sm_count, int f
                             int ctas_per_sm = 2);
 cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, bool bf, bool group, int out_dtype,
                              const SkinnyTcPlan &p, cudaStream_t st, bool pdl);
+// SiLU-gated gate/up product: a.N = 2 * a.nh stacked rows, out [M, nh]; plan with
+// plan_skinny_tc(M, 2 * nh, K, ...) (64 row pairs per CTA = 128 rows)
+cudaError_t launch_skinny_silu(const SkinnyTcArgs &a, bool bf, bool group, int out_dtype,
+                               const SkinnyTcPlan &p, cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------ tile path
 struct TileArgs {

@@ -61,3 +61,44 @@ def check(y_gpu: torch.Tensor, y_ref: np.ndarray, x: torch.Tensor, scale: torch.
     lim = REL_L2 + UNIT_ROUNDOFF[y_gpu.dtype]
     assert rel <= lim, f"{what}: relative L2 {rel:.3g} > {lim:.3g}"
     return rel, ratio
+
+
+def silu_refs(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor, group_size: int,
+              nthreads: int = 8):
+    """Oracle h = silu(g) * u and the oracle's g, u (fp64) for a stacked gate/up layer."""
+    p = packed.detach().cpu().numpy()
+    sb = bits(scale)
+    xb = bits(x)
+    h = oracle.silu_mul_from_bits(xb, x_dtype_name(x.dtype), p, sb, group_size, nthreads)
+    y = oracle.linear_from_bits(xb, x_dtype_name(x.dtype), p, sb, group_size, nthreads)
+    n = p.shape[0] // 2
+    return h, y[:, :n], y[:, n:]
+
+
+def check_silu(h_gpu: torch.Tensor, h_ref: np.ndarray, g_ref: np.ndarray, u_ref: np.ndarray,
+               x: torch.Tensor, scale: torch.Tensor, what=""):
+    """Tolerance of the gated product, propagated from the linear's: with E the
+    per-element bound of g and u (2e-3 * s_max * sum|x|) and |silu'| <= 1.1,
+    |dh| <= 1.1 E |u| + |silu(g)| E + 1.1 E^2, plus 1e-5 |h| for the fp32
+    exp / divide / multiply and half an ulp of a 16-bit output; relative L2
+    <= 1e-4 (+ unit roundoff of the output dtype)."""
+    h = h_gpu.detach().float().cpu().numpy().astype(np.float64)
+    assert h.shape == h_ref.shape, (h.shape, h_ref.shape)
+    assert np.all(np.isfinite(h)), f"{what}: non-finite output"
+    s = scale.detach().float().cpu().numpy().astype(np.float64)
+    smax = np.abs(s).reshape(s.shape[0], -1).max(axis=1)
+    n = g_ref.shape[1]
+    sm = np.maximum(smax[:n], smax[n:])
+    xabs = np.abs(x.detach().float().cpu().numpy().astype(np.float64)).sum(axis=1)
+    E = PER_ELEM * xabs[:, None] * sm[None, :]
+    silu_g = g_ref / (1.0 + np.exp(-g_ref))
+    bound = (1.1 * E * np.abs(u_ref) + np.abs(silu_g) * E + 1.1 * E * E + 1e-5 * np.abs(h_ref)
+             + 0.5 * ulp(h_ref, h_gpu.dtype))
+    err = np.abs(h - h_ref)
+    ratio = float(np.max(err / np.maximum(bound, 1e-300))) if err.size else 0.0
+    assert np.all(err <= bound), f"{what}: per-element bound exceeded (max ratio {ratio:.3g})"
+    den = float(np.linalg.norm(h_ref))
+    rel = float(np.linalg.norm(h - h_ref)) / den if den > 0 else float(np.linalg.norm(h))
+    lim = REL_L2 + UNIT_ROUNDOFF[h_gpu.dtype]
+    assert rel <= lim, f"{what}: relative L2 {rel:.3g} > {lim:.3g}"
+    return rel, ratio

@@ -105,6 +105,32 @@ def test_linear_empty_is_noop(lib):
     assert lin(lib, N=0, packed=0, scale=0, out=0) == TL_OK
 
 
+def silu(lib, x=A, xdt=1, packed=B, scale=C, gs=0, out=D, odt=2, M=4, N=8, K=128, flags=0):
+    lib.ternary_linear_silu_mul.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                            ctypes.c_int32, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_uint32, ctypes.c_void_p]
+    return lib.ternary_linear_silu_mul(ctypes.c_void_p(x), xdt, ctypes.c_void_p(packed),
+                                       ctypes.c_void_p(scale), gs, ctypes.c_void_p(out), odt,
+                                       M, N, K, flags, None)
+
+
+def test_silu_mul_argument_errors(lib):
+    # checked on the host before any device work
+    assert silu(lib, M=33) == TL_ERR_UNSUPPORTED      # decode shapes only
+    assert silu(lib, gs=64) == TL_ERR_UNSUPPORTED     # 64-wide groups: tile kernel only
+    assert silu(lib, gs=32) == TL_ERR_DTYPE
+    assert silu(lib, flags=4) == TL_ERR_DTYPE
+    assert silu(lib, N=-1) == TL_ERR_SHAPE
+    assert silu(lib, K=130) == TL_ERR_SHAPE
+    assert silu(lib, gs=256, K=384) == TL_ERR_SHAPE
+    assert silu(lib, K=96) == TL_ERR_ALIGN
+    assert silu(lib, out=0) == TL_ERR_NULL
+    assert silu(lib, packed=B + 1) == TL_ERR_ALIGN
+    assert silu(lib, M=0, x=0, out=0) == TL_OK         # empty: no-op
+    assert silu(lib, N=0, packed=0, scale=0, out=0) == TL_OK
+
+
 def test_packing_argument_errors(lib):
     p = ctypes.c_void_p
     assert lib.ternary_pack(p(A), p(B), 4, 6, None, None) == TL_ERR_SHAPE

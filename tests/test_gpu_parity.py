@@ -14,7 +14,7 @@ import ternary_weight_linear_02_gb300 as tl
 from ternary_weight_linear_02_gb300 import synth
 from ternary_weight_linear_02_gb300.workloads import CONFIGS
 
-from parity import check, oracle_ref
+from parity import check, check_silu, oracle_ref, silu_refs
 
 pytestmark = pytest.mark.gpu
 
@@ -338,6 +338,52 @@ def test_linear_group256(M, N, K, xdt, odt):
     torch.cuda.synchronize()
     check(y, oracle_ref(x, p, s, 256), x, s, what=f"g256 {M}x{N}x{K}")
     assert tl.device_status() == 0
+
+
+# ------------------------------------------------------------------ SiLU-gated gate/up
+SILU = [
+    # M, N (output columns = gate rows = up rows), K, x dtype, out dtype, group size
+    (1, 300, 1024, torch.bfloat16, torch.float32, 0),      # split K over 8 CTAs
+    (2, 4096, 4096, torch.bfloat16, torch.float32, 0),     # M = 2 on the tcgen05 kernel
+    (3, 64, 640, torch.float16, torch.float16, 0),         # split K 5: uneven pair slices
+    (4, 1000, 2048, torch.float16, torch.float32, 128),
+    (7, 100, 8192, torch.bfloat16, torch.float32, 128),    # ragged last pair tile
+    (16, 11008, 4096, torch.bfloat16, torch.bfloat16, 0),  # 7B gate/up, no split K
+    (32, 256, 4096, torch.bfloat16, torch.float32, 256),   # 32 tokens, 256-wide groups
+]
+
+
+@pytest.mark.parametrize("M,N,K,xdt,odt,gs", SILU)
+def test_linear_silu_mul(M, N, K, xdt, odt, gs):
+    x, p, s = layer_inputs(M, 2 * N, K, xdt, gs, 6, p_reserved=0.001)
+    h = tl.linear_silu_mul(x, p, s, gs, out_dtype=odt, static_weights=True)
+    torch.cuda.synchronize()
+    h_ref, g_ref, u_ref = silu_refs(x, p, s, gs)
+    check_silu(h, h_ref, g_ref, u_ref, x, s, what=f"silu {M}x{N}x{K} g{gs}")
+    assert tl.device_status() == 0
+
+
+def test_silu_mul_matches_unfused_calls():
+    """The fused call equals silu(g) * u formed from the plain kernel's fp32 g and u."""
+    M, N, K = 5, 640, 3072
+    x, p, s = layer_inputs(M, 2 * N, K, torch.bfloat16, 128, 7)
+    h = tl.linear_silu_mul(x, p, s, 128, out_dtype=torch.float32)
+    y = tl.linear(x, p, s, 128, out_dtype=torch.float32)
+    g, u = y[:, :N], y[:, N:]
+    want = torch.nn.functional.silu(g) * u
+    torch.cuda.synchronize()
+    assert torch.allclose(h, want, rtol=1e-5, atol=1e-6 * float(want.abs().max()))
+
+
+def test_silu_mul_refusals():
+    x, p, s = layer_inputs(33, 128, 256, torch.bfloat16, 0, 8)
+    with pytest.raises(tl.TernaryError) as e:
+        tl.linear_silu_mul(x, p, s, 0)
+    assert e.value.status == 8  # TL_ERR_UNSUPPORTED: decode shapes only
+    x, p, s = layer_inputs(4, 128, 256, torch.bfloat16, 64, 8)
+    with pytest.raises(tl.TernaryError) as e:
+        tl.linear_silu_mul(x, p, s, 64)
+    assert e.value.status == 8
 
 
 def test_group64_skinny_path_refused():

@@ -259,6 +259,65 @@ def test_fused_rows_equal_shards(oracle_mod):
         off += p.shape[0]
 
 
+# ---------------------------------------------------------------- SiLU-gated product
+def _negate_codes(packed):
+    """Swap codes 01 and 10 in every field: the same weights with the sign flipped."""
+    b = packed.astype(np.uint16)
+    out = np.zeros_like(b)
+    for j in range(4):
+        c = (b >> (2 * j)) & 3
+        c = np.where(c == 1, 2, np.where(c == 2, 1, c))
+        out |= c << (2 * j)
+    return out.astype(np.uint8)
+
+
+@pytest.mark.parametrize("group_size", [0, 128])
+def test_silu_mul_odd_part_is_the_plain_product(oracle_mod, group_size):
+    """silu(g) - silu(-g) = g for every g, so h(gate) - h(-gate) = g * u: pins the
+    sign inside exp, which shard is the gate, and the rows' order."""
+    rng = np.random.default_rng(23)
+    M, N, K = 4, 7, 256
+    x = rng.standard_normal((M, K))
+    gate = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    up = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    ss = (2 * N,) if group_size == 0 else (2 * N, K // group_size)
+    s = rng.uniform(0.2, 1.0, size=ss)
+    h1 = oracle_mod.silu_mul_f64(x, np.concatenate([gate, up]), s, group_size)
+    h2 = oracle_mod.silu_mul_f64(x, np.concatenate([_negate_codes(gate), up]), s, group_size)
+    g = oracle_mod.linear_f64(x, gate, s[:N], group_size)
+    u = oracle_mod.linear_f64(x, up, s[N:], group_size)
+    np.testing.assert_allclose(h1 - h2, g * u, rtol=1e-12, atol=1e-12)
+
+
+def test_silu_mul_point_values(oracle_mod):
+    """One-hot weights give g = x_a, u = x_b: h = sigma(x_a) x_a x_b, checked at
+    sigma(1) = 1 / (1 + 1/e) = 0.7310585786300049 and at g = 0 and g >> 0."""
+    K = 64
+    x = np.zeros((3, K))
+    x[0, 0], x[0, 1] = 1.0, 2.0      # g = 1, u = 2
+    x[1, 0], x[1, 1] = 0.0, 5.0      # g = 0: h = 0
+    x[2, 0], x[2, 1] = 60.0, -0.5    # g = 60: silu(g) = g to 1e-24 relative
+    t = np.zeros((2, K), dtype=np.int8)
+    t[0, 0] = 1   # gate row reads x[:, 0]
+    t[1, 1] = 1   # up row reads x[:, 1]
+    packed, _ = oracle_mod.pack(t)
+    h = oracle_mod.silu_mul_f64(x, packed, np.ones(2), 0)
+    assert abs(h[0, 0] - 2.0 * 0.7310585786300049) < 1e-15
+    assert h[1, 0] == 0.0
+    assert abs(h[2, 0] - (-30.0)) < 1e-12
+
+
+def test_silu_mul_zero_up_or_gate(oracle_mod):
+    rng = np.random.default_rng(29)
+    M, N, K = 2, 5, 128
+    x = rng.standard_normal((M, K))
+    gate = rng.integers(0, 256, size=(N, K // 4), dtype=np.uint8)
+    zero = np.zeros((N, K // 4), dtype=np.uint8)
+    s = np.ones(2 * N)
+    assert np.all(oracle_mod.silu_mul_f64(x, np.concatenate([gate, zero]), s, 0) == 0.0)
+    assert np.all(oracle_mod.silu_mul_f64(x, np.concatenate([zero, gate]), s, 0) == 0.0)
+
+
 def test_threads_do_not_change_results(oracle_mod):
     rng = np.random.default_rng(19)
     x = rng.standard_normal((3, 384))
