@@ -142,13 +142,14 @@ tl_status ternary_linear_ex(const void *x, int32_t x_dtype, const uint8_t *packe
  *   out[m, j] = silu(g[m, j]) * u[m, j],  silu(v) = v / (1 + exp(-v)),  j < N
  * The stacked layout is the fused gate/up layer of ternary_linear (shards at
  * row offsets 0 and N; "三元量化模型接入vLLM…完整实战" §3.2).
- *   packed: [2N, K/4]; scale: fp16 [2N] (group_size 0) or [2N, K/G] (G = 128
- *   or 256); out: [M, N] in out_dtype; g and u are fp32 (scaled) and the
+ *   packed: [2N, K/4]; scale: fp16 [2N] (group_size 0) or [2N, K/G] (G = 64,
+ *   128 or 256); out: [M, N] in out_dtype; g and u are fp32 (scaled) and the
  *   product is computed in fp32, then rounded to out_dtype.
  *   flags: TL_FLAG_STATIC_WEIGHTS or 0.
- * Served by the decode kernel: M > 32 or group_size 64 return
- * TL_ERR_UNSUPPORTED; other argument errors as ternary_linear (with 2N rows).
- * N == 0 or M == 0 is a no-op; K == 0 writes zeros.  Asynchronous on stream.
+ * Decode shapes (M <= ternary_skinny_max_m(), G != 64) run on the decode
+ * kernel, the rest on the tile kernel, each with the product in its epilogue.
+ * Argument errors as ternary_linear (with 2N rows).  N == 0 or M == 0 is a
+ * no-op; K == 0 writes zeros.  Asynchronous on stream.
  */
 tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed,
                                   const void *scale, int32_t group_size, void *out,

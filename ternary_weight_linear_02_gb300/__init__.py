@@ -219,8 +219,7 @@ def linear_silu_mul(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
     """silu(g) * u for a fused gate/up layer, in one kernel.
 
     ``packed`` [2N, K/4] and ``scale`` ([2N] or [2N, K/G]) stack the gate rows
-    then the up rows; g = x @ gate^T, u = x @ up^T; returns [..., N].  Decode
-    shapes only (M <= 32 tokens after flattening the leading dimensions).
+    then the up rows; g = x @ gate^T, u = x @ up^T; returns [..., N].
     """
     _need_cuda(x, packed, scale, out)
     if x.dtype not in (torch.float16, torch.bfloat16):

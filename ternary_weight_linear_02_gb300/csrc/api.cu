@@ -249,7 +249,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
 }
 
 // Fused gate/up with the SiLU-gated product: packed / scale hold 2N stacked rows
-// (gate, then up), out is [M, N].  Served by the tcgen05 decode kernel only.
+// (gate, then up), out is [M, N].  Decode shapes run on the tcgen05 decode
+// kernel, larger M (and 64-wide groups) on the tile kernel.
 tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
                        int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
                        int64_t K, uint32_t flags, void *stream) {
@@ -259,7 +260,6 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
                                &noop);
     if (s != TL_OK || noop) return s;
     if (flags & ~(uint32_t)TL_FLAG_STATIC_WEIGHTS) return TL_ERR_DTYPE;
-    if (M > 32 || group_size == 64) return TL_ERR_UNSUPPORTED;
     if (take_injected_failure()) return TL_ERR_CUDA;
     DevInfo *d = nullptr;
     s = current_device(&d, true);
@@ -267,11 +267,31 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // K == 0: g = u = 0 and silu(0) * 0 = 0
     if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)(M * N) * dtype_size(out_dtype), st));
-    static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
-    static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
-    tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, 2 * N, K, d->sm_count, force_sk, per_sm);
-    if (!tp.ok) return TL_ERR_UNSUPPORTED;
-    tl::SkinnyTcArgs a{};
+    const bool bf = x_dtype == TL_BF16;
+    const bool group = group_size != 0;
+    const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
+    if (M <= skinny_max_m() && group_size != 64) {
+        static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
+        static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
+        tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, 2 * N, K, d->sm_count, force_sk, per_sm);
+        if (tp.ok) {
+            tl::SkinnyTcArgs a{};
+            a.x = static_cast<const uint16_t *>(x);
+            a.packed = packed;
+            a.scale = static_cast<const uint16_t *>(scale);
+            a.out = out;
+            a.M = (int)M;
+            a.N = (int)(2 * N);
+            a.K = (int)K;
+            a.nh = (int)N;
+            a.gshift = gshift;
+            a.flags = skinny_launch_flags(flags);
+            a.status = d->status;
+            return from_cuda(tl::launch_skinny_silu(a, bf, group, out_dtype, tp, st, pdl_enabled()));
+        }
+    }
+    if (!tl::tile_supported(M, 2 * N, K)) return TL_ERR_UNSUPPORTED;
+    tl::TileArgs a{};
     a.x = static_cast<const uint16_t *>(x);
     a.packed = packed;
     a.scale = static_cast<const uint16_t *>(scale);
@@ -280,11 +300,9 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     a.N = (int)(2 * N);
     a.K = (int)K;
     a.nh = (int)N;
-    a.gshift = group_size == 256 ? 8 : 7;
-    a.flags = skinny_launch_flags(flags);
+    a.gshift = gshift;
     a.status = d->status;
-    return from_cuda(tl::launch_skinny_silu(a, x_dtype == TL_BF16, group_size != 0, out_dtype, tp, st,
-                                            pdl_enabled()));
+    return from_cuda(tl::launch_tile_silu(a, bf, group, out_dtype, st, pdl_enabled()));
 }
 
 tl_status check_packing(const void *t, const void *packed, int64_t N, int64_t K,

@@ -1,350 +1,8 @@
-// kern_tile.cu -- large-M ternary linear on the 5th-generation tensor cores.
-//
-// out[m,n] = sum_k t[n,k] x[m,k] with a per-channel scale (Qwen2.5-7B
-// ternary-in-vLLM write-up, m.nxbn.cn/news/169761, §3.2, §4.2) or a
-// per-128-wide-K-group scale ("三元量化模型接入vLLM：从逆向加载到Kernel优化的完整实战",
-// trdm.cn/news/729035, §3.1, §4.2) -- or 64-wide groups, the variant of the
-// "Bonsai 2 27B" port (m.xxqk.cn/news/593501, §4.2, §5.2); codes decoded with
-// the table of the first page's §3.1.  The scale is applied per 64-k chunk, so
-// either group size is one chunk or two.
-//
-// One CTA computes a 128 (weight rows n) x BN (tokens m) output tile:
-//   D[n, m] = sum_k A[n, k] B[k, m],  A = decoded weights, B = x^T.
-//  * Warps 0-3 (one thread per weight row = one TMEM lane) read their row's
-//    packed codes from global memory, decode 64 codes per chunk into 32
-//    registers of bf16x2 / f16x2 and store them into a TMEM A stage with
-//    tcgen05.st.  The decoded weights never touch shared memory.
-//  * Warp 4 streams x tiles (BN x 64 k, natural K order) into a 4-stage
-//    shared-memory ring with TMA (128-byte swizzle).
-//  * Warp 5 allocates TMEM and issues tcgen05.mma (kind::f16, A from TMEM,
-//    B from shared memory, fp32 accumulator D in TMEM), committing each chunk
-//    to the barriers that free its A stage and x stage.
-//  * Epilogue: warps 0-3 read D with tcgen05.ld, apply the scale, convert and
-//    store; a warp's 32 lanes write 32 consecutive n of one token row.
-// Weight decode: 2*t in {+-2, +-0}, exact in both 16-bit formats, so every
-// product is exact and the fp32 accumulation performs the same signed sums as
-// the add / subtract / skip formulation.  Scales:
-//   per channel        -> out = 0.5 * s[n] * D
-//   per group, fp16 x  -> A holds t*s[n,g] exactly (s is fp16)
-//   per group, bf16 x  -> s = s_hi + s_lo with both parts exact in bf16; two
-//                         MMAs per k step (A_hi and A_lo) into the same D.
-// Every mbarrier wait is bounded; a wait that gives up sets the device status
-// word, the CTA stops issuing work, frees its TMEM and returns.
-#include <cuda.h>
-
-#include "kernels.h"
-#include "tc.cuh"
+// kern_tile.cu -- large-M ternary linear on the tensor cores: support check and
+// the plain-output entry point.  The kernel itself is in tile.cuh.
+#include "tile.cuh"
 
 namespace tl {
-
-namespace {
-
-constexpr int kKC = 64;   // k per pipeline chunk = one 128-byte row of x
-constexpr int kNS = 4;    // x stages in shared memory
-constexpr int kThreads = 192;
-
-enum { kChannel = 0, kFold = 1, kSplit = 2 };
-
-__host__ __device__ constexpr uint32_t pow2ceil(uint32_t v) {
-    uint32_t p = 32;
-    while (p < v) p <<= 1;
-    return p;
-}
-
-template <int BN, int SMODE>
-struct TileCfg {
-    static constexpr int ACOLS = (SMODE == kSplit) ? 64 : 32;  // TMEM columns per A stage
-    static constexpr int NA = (SMODE == kSplit) ? 3 : 4;       // A stages
-    static constexpr uint32_t TMEM_COLS = pow2ceil(NA * ACOLS + BN);
-    static constexpr int XSTAGE = BN * 128;                    // bytes per x stage
-    // shared memory: [x stages][barriers][tmem slot, abort flag] + 1 KB alignment slack
-    static constexpr int BAR_OFF = kNS * XSTAGE;
-    static constexpr int NBARS = 2 * kNS + 2 * NA + 1;
-    static constexpr int SMEM = BAR_OFF + NBARS * 8 + 16 + 1024;
-};
-
-// Adjacent-pair decode of one 32-bit word of 16 codes (k = 0..15 of the word)
-// into 8 registers, register p = {2*t[2p], 2*t[2p+1]} (low half = lower k):
-// after sign_nz, nibble p holds the two codes as (b1, nz) pairs; isolating the
-// nibble and multiplying by 2^(14-4p) + 2^(28-4p) places code 2p at bits
-// 15:14 and code 2p+1 at bits 31:30 (the two partial products do not overlap).
-__device__ __forceinline__ void decode_word_adjacent(uint32_t w, uint32_t *r) {
-    const uint32_t z = sign_nz(w);
-    const uint32_t zh = z >> 16;
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const uint32_t mul = (1u << (14 - 4 * p)) + (1u << (28 - 4 * p));
-        r[p] = ((z & (0xFu << (4 * p))) * mul) & 0xC000C000u;
-        r[p + 4] = ((zh & (0xFu << (4 * p))) * mul) & 0xC000C000u;
-    }
-}
-
-template <int BN, bool BF, int SMODE, int OUT>
-__global__ void __launch_bounds__(kThreads, 1)
-    tile_tc_kernel(const __grid_constant__ CUtensorMap tmx, TileArgs a) {
-    using C = TileCfg<BN, SMODE>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                ~static_cast<uintptr_t>(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *xfull = bars, *xempty = bars + kNS;
-    uint64_t *afull = bars + 2 * kNS, *aempty = afull + C::NA;
-    uint64_t *dfull = aempty + C::NA;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBARS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * 128, m0 = blockIdx.y * BN;
-    const int nchunks = a.K / kKC;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kNS; ++i) {
-            mbar_init(&xfull[i], 1);
-            mbar_init(&xempty[i], 1);
-        }
-        for (int i = 0; i < C::NA; ++i) {
-            mbar_init(&afull[i], 4);  // one arrival per decoder warp
-            mbar_init(&aempty[i], 1);
-        }
-        mbar_init(dfull, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    if (warp == 5) tc::tmem_alloc(tmem_slot, C::TMEM_COLS);
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t dcol = tmem + (uint32_t)(C::NA * C::ACOLS);
-
-    pdl_launch_dependents();
-    pdl_wait();  // x / packed / out may be produced / consumed by the previous kernel
-
-    auto give_up = [&]() {
-        *abort_flag = 1;
-        if (a.status) atomicExch(a.status, kStatusTimeout);
-    };
-
-    if (warp == 4) {
-        // ---------------- TMA producer: x tiles
-        if (lane == 0) {
-            tc::prefetch_tmap(&tmx);
-            for (int c = 0; c < nchunks && !*abort_flag; ++c) {
-                const int s = c % kNS;
-                if (c >= kNS && !mbar_wait_bounded(&xempty[s], ((c / kNS) - 1) & 1)) {
-                    give_up();
-                    break;
-                }
-                mbar_arrive_expect_tx(&xfull[s], (uint32_t)C::XSTAGE);
-                tc::tma_load_2d(smem + (size_t)s * C::XSTAGE, &tmx, c * kKC, m0, &xfull[s]);
-            }
-        }
-    } else if (warp == 5) {
-        // ---------------- MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16(BN, BF);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % C::NA, xs = c % kNS;
-                if (*abort_flag || !mbar_wait_bounded(&afull[s], (c / C::NA) & 1) ||
-                    !mbar_wait_bounded(&xfull[xs], (c / kNS) & 1)) {
-                    give_up();
-                    break;
-                }
-                tc::fence_after_sync();
-                const uint64_t bdesc = tc::desc_sw128(smem + (size_t)xs * C::XSTAGE);
-                const uint32_t acol = tmem + (uint32_t)(s * C::ACOLS);
-#pragma unroll
-                for (int kk = 0; kk < kKC / 16; ++kk) {
-                    const uint64_t b = bdesc + (uint64_t)(kk * 2);  // +32 B per 16 elements
-                    tc::mma_ts(dcol, acol + kk * 8, b, idesc, (c | kk) != 0);
-                    if constexpr (SMODE == kSplit) tc::mma_ts(dcol, acol + 32 + kk * 8, b, idesc, 1);
-                }
-                tc::commit(&aempty[s]);
-                tc::commit(&xempty[xs]);
-            }
-            tc::commit(dfull);
-        }
-    } else {
-        // ---------------- decoders / epilogue: thread = weight row = TMEM lane
-        const int row = warp * 32 + lane;
-        const int n = n0 + row;
-        const bool rowok = n < a.N;
-        const int64_t Kq = a.K >> 2;
-        const uint8_t *prow = a.packed + (int64_t)(rowok ? n : 0) * Kq;
-        const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-        const int ngk = a.K >> a.gshift;  // scale groups per row (G = 64, 128 or 256)
-        const uint16_t *srow = a.scale + (SMODE == kChannel ? 0 : (int64_t)(rowok ? n : 0) * ngk);
-
-        uint4 cur = rowok && nchunks > 0 ? *reinterpret_cast<const uint4 *>(prow) : make_uint4(0, 0, 0, 0);
-        uint4 nxt = rowok && nchunks > 1 ? *reinterpret_cast<const uint4 *>(prow + 16)
-                                         : make_uint4(0, 0, 0, 0);
-        bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % C::NA;
-            const uint4 codes = cur;
-            cur = nxt;
-            if (rowok && c + 2 < nchunks)
-                nxt = *reinterpret_cast<const uint4 *>(prow + (size_t)(c + 2) * 16);
-            uint32_t r[32];
-            decode_word_adjacent(codes.x, r + 0);
-            decode_word_adjacent(codes.y, r + 8);
-            decode_word_adjacent(codes.z, r + 16);
-            decode_word_adjacent(codes.w, r + 24);
-            uint32_t rl[32];
-            if constexpr (SMODE != kChannel) {
-                const uint16_t sbits = rowok ? srow[(c * kKC) >> a.gshift] : (uint16_t)0;
-                const float sf = h2f(sbits);
-                if constexpr (SMODE == kFold) {
-                    // fp16: (+-2) * (s/2) = +-s exactly
-                    const __half2 h2 = __half2half2(__float2half_rn(0.5f * sf));
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        __half2 v = *reinterpret_cast<__half2 *>(&r[i]);
-                        v = __hmul2(v, h2);
-                        r[i] = *reinterpret_cast<uint32_t *>(&v);
-                    }
-                } else {
-                    // bf16: s = s_hi + s_lo, both exact in bf16
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(sf);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(sf - __bfloat162float(hi));
-                    const __nv_bfloat162 h2 =
-                        __bfloat162bfloat162(__float2bfloat16_rn(0.5f * __bfloat162float(hi)));
-                    const __nv_bfloat162 l2 =
-                        __bfloat162bfloat162(__float2bfloat16_rn(0.5f * __bfloat162float(lo)));
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r[i]);
-                        __nv_bfloat162 vh = __hmul2(v, h2), vl = __hmul2(v, l2);
-                        r[i] = *reinterpret_cast<uint32_t *>(&vh);
-                        rl[i] = *reinterpret_cast<uint32_t *>(&vl);
-                    }
-                }
-            }
-            // wait results are made warp-uniform: tcgen05.st below is warp-collective
-            if (c >= C::NA) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&aempty[s], ((c / C::NA) - 1) & 1));
-            if (!ok) give_up();
-            if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
-                ok = false;
-                break;
-            }
-            tc::st_32x32b_x32(tlane + (uint32_t)(s * C::ACOLS), r);
-            if constexpr (SMODE == kSplit) tc::st_32x32b_x32(tlane + (uint32_t)(s * C::ACOLS + 32), rl);
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[s]);
-        }
-        // ---------------- epilogue
-        ok = __all_sync(0xffffffffu, ok);
-        const bool ready = ok && __all_sync(0xffffffffu, mbar_wait_bounded(dfull, 0));
-        if (ready) {
-            tc::fence_after_sync();
-            // channel mode: A held 2*t, so D = 2*sum(t x); group modes: A held t*s
-            float sc = 1.f;
-            if constexpr (SMODE == kChannel) sc = 0.5f * (rowok ? h2f(a.scale[n]) : 0.f);
-#pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t d[32];
-                tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
-                tc::wait_ld();
-                if (rowok) {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int m = m0 + j * 32 + q;
-                        if (m < a.M)
-                            OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, __uint_as_float(d[q]) * sc);
-                    }
-                }
-            }
-        } else if (ok) {
-            give_up();
-        }
-    }
-
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (warp == 5) tc::tmem_dealloc(tmem, C::TMEM_COLS);
-}
-
-// ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                             cudaEnableDefault, &q) != cudaSuccess ||
-            q != cudaDriverEntryPointSuccess) {
-            cudaGetLastError();
-            p = nullptr;
-        }
-        return reinterpret_cast<EncodeTiledFn>(p);
-    }();
-    return fn;
-}
-
-template <int BN, bool BF, int SMODE, int OUT>
-cudaError_t launch_one(const TileArgs &a, cudaStream_t st, bool pdl) {
-    using C = TileCfg<BN, SMODE>;
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return cudaErrorNotSupported;
-    CUtensorMap map;
-    const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)BN};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&map, BF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                     const_cast<uint16_t *>(a.x), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = tile_tc_kernel<BN, BF, SMODE, OUT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.N + 127) / 128), (unsigned)((a.M + BN - 1) / BN), 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    int na = 0;
-    if (pdl) {
-        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
-    }
-    cfg.attrs = attr;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, map, a);
-}
-
-template <int BN, bool BF, int SMODE>
-cudaError_t launch_out(const TileArgs &a, int out_dtype, cudaStream_t st, bool pdl) {
-    switch (out_dtype) {
-    case 0: return launch_one<BN, BF, SMODE, 0>(a, st, pdl);
-    case 1: return launch_one<BN, BF, SMODE, 1>(a, st, pdl);
-    default: return launch_one<BN, BF, SMODE, 2>(a, st, pdl);
-    }
-}
-
-template <int BN>
-cudaError_t launch_bn(const TileArgs &a, bool bf, bool group, int out_dtype, cudaStream_t st,
-                      bool pdl) {
-    if (!group)
-        return bf ? launch_out<BN, true, kChannel>(a, out_dtype, st, pdl)
-                  : launch_out<BN, false, kChannel>(a, out_dtype, st, pdl);
-    return bf ? launch_out<BN, true, kSplit>(a, out_dtype, st, pdl)
-              : launch_out<BN, false, kFold>(a, out_dtype, st, pdl);
-}
-
-}  // namespace
-
-int tile_bn_for(int64_t M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
 
 bool tile_supported(int64_t M, int64_t N, int64_t K) {
     return M >= 1 && N >= 1 && K >= 64 && K % 64 == 0 && encode_fn() != nullptr;
@@ -352,11 +10,7 @@ bool tile_supported(int64_t M, int64_t N, int64_t K) {
 
 cudaError_t launch_tile(const TileArgs &a, bool bf, bool group, int out_dtype, int /*sm_count*/,
                         cudaStream_t st, bool pdl) {
-    switch (tile_bn_for(a.M)) {
-    case 64: return launch_bn<64>(a, bf, group, out_dtype, st, pdl);
-    case 128: return launch_bn<128>(a, bf, group, out_dtype, st, pdl);
-    default: return launch_bn<256>(a, bf, group, out_dtype, st, pdl);
-    }
+    return launch_tile_any<false>(a, bf, group, out_dtype, st, pdl);
 }
 
 }  // namespace tl

@@ -1,0 +1,13 @@
+// kern_tile_silu.cu -- large-M fused gate/up projection with the SiLU-gated
+// product, out[m, j] = silu(g[m, j]) * u[m, j]; the kernel in tile.cuh with
+// SILU = true (64 gate rows and the matching 64 up rows per CTA).
+#include "tile.cuh"
+
+namespace tl {
+
+cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype,
+                             cudaStream_t st, bool pdl) {
+    return launch_tile_any<true>(a, bf, group, out_dtype, st, pdl);
+}
+
+}  // namespace tl

@@ -99,12 +99,16 @@ struct TileArgs {
     const uint16_t *scale;   // fp16 [N] or [N,K/G]
     void *out;               // [M,N]
     int M, N, K;
-    int gshift;              // log2 of the group size G (6 or 7) in group mode
+    int gshift;              // log2 of the group size G (6, 7 or 8) in group mode
+    int nh;                  // SiLU-gated call: gate rows [0, nh), up rows [nh, 2 nh), out [M, nh]
     int *status;             // device status word (bounded-wait failures)
 };
 
 bool tile_supported(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_tile(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
                         cudaStream_t st, bool pdl);
+// SiLU-gated gate/up product on the tile kernel: a.N = 2 * a.nh stacked rows, out [M, nh]
+cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype,
+                             cudaStream_t st, bool pdl);
 
 }  // namespace tl

@@ -350,6 +350,11 @@ SILU = [
     (7, 100, 8192, torch.bfloat16, torch.float32, 128),    # ragged last pair tile
     (16, 11008, 4096, torch.bfloat16, torch.bfloat16, 0),  # 7B gate/up, no split K
     (32, 256, 4096, torch.bfloat16, torch.float32, 256),   # 32 tokens, 256-wide groups
+    (4, 320, 1024, torch.float16, torch.float32, 64),      # 64-wide groups: tile kernel
+    (33, 300, 1024, torch.bfloat16, torch.float32, 0),     # tile kernel from here on
+    (100, 1000, 2048, torch.float16, torch.float16, 128),
+    (300, 384, 2048, torch.bfloat16, torch.float32, 128),
+    (1024, 512, 1024, torch.bfloat16, torch.bfloat16, 0),  # BN = 256 tiles
 ]
 
 
@@ -375,15 +380,14 @@ def test_silu_mul_matches_unfused_calls():
     assert torch.allclose(h, want, rtol=1e-5, atol=1e-6 * float(want.abs().max()))
 
 
-def test_silu_mul_refusals():
-    x, p, s = layer_inputs(33, 128, 256, torch.bfloat16, 0, 8)
-    with pytest.raises(tl.TernaryError) as e:
-        tl.linear_silu_mul(x, p, s, 0)
-    assert e.value.status == 8  # TL_ERR_UNSUPPORTED: decode shapes only
-    x, p, s = layer_inputs(4, 128, 256, torch.bfloat16, 64, 8)
-    with pytest.raises(tl.TernaryError) as e:
-        tl.linear_silu_mul(x, p, s, 64)
-    assert e.value.status == 8
+def test_silu_mul_tile_matches_unfused_calls():
+    M, N, K = 200, 384, 2048
+    x, p, s = layer_inputs(M, 2 * N, K, torch.float16, 0, 9)
+    h = tl.linear_silu_mul(x, p, s, 0, out_dtype=torch.float32)
+    y = tl.linear(x, p, s, 0, out_dtype=torch.float32)
+    want = torch.nn.functional.silu(y[:, :N]) * y[:, N:]
+    torch.cuda.synchronize()
+    assert torch.allclose(h, want, rtol=1e-5, atol=1e-6 * float(want.abs().max()))
 
 
 def test_group64_skinny_path_refused():
