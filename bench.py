@@ -167,6 +167,55 @@ class Stack:
                               out=self.out[M][d][j], static_weights=True)
 
 
+class FusedStack:
+    """The same weights in the fused layout a vLLM-style model runs: per layer
+    one QKV call (q, k, v rows stacked), o, one gate/up call with the SiLU-gated
+    product in its epilogue (ternary_linear_silu_mul), and down reading that
+    product -- 4 calls per layer instead of 7, the same packed bytes."""
+
+    NAMES = ("q", "k", "v", "o", "gate", "up", "down")
+
+    def __init__(self, stack):
+        cfg = stack.cfg
+        names = [l.name for l in cfg.layers]
+        self.ok = all(n in names for n in self.NAMES)
+        if not self.ok:
+            return
+        ix = {n: i for i, n in enumerate(names)}
+        self.cfg, self.stack = cfg, stack
+        self.w = []
+        for d in range(cfg.depth):
+            w = stack.w[d]
+            qkv = tuple(torch.cat([w[ix[n]][t] for n in "qkv"]) for t in (0, 1))
+            gu = tuple(torch.cat([w[ix["gate"]][t], w[ix["up"]][t]]) for t in (0, 1))
+            self.w.append((qkv, w[ix["o"]], gu, w[ix["down"]]))
+        self.ix = ix
+        self.bufs = {}
+        for M in stack.Ms:
+            layer = []
+            for d in range(cfg.depth):
+                qkv_n = self.w[d][0][0].shape[0]
+                o_n = self.w[d][1][0].shape[0]
+                h_n = self.w[d][2][0].shape[0] // 2
+                dn_n = self.w[d][3][0].shape[0]
+                layer.append(tuple(torch.empty((M, n), dtype=cfg.x_dtype, device=stack.dev)
+                                   for n in (qkv_n, o_n, h_n, dn_n)))
+            self.bufs[M] = layer
+
+    def calls_per_layer(self):
+        return 4
+
+    def run_m(self, tl, M):
+        cfg, st, ix = self.cfg, self.stack, self.ix
+        for d in range(cfg.depth):
+            (qkv, o, gu, dn), (y_qkv, y_o, h, y_dn) = self.w[d], self.bufs[M][d]
+            gs = cfg.group_size
+            tl.linear(st.x[M][d][ix["q"]], qkv[0], qkv[1], gs, out=y_qkv, static_weights=True)
+            tl.linear(st.x[M][d][ix["o"]], o[0], o[1], gs, out=y_o, static_weights=True)
+            tl.linear_silu_mul(st.x[M][d][ix["gate"]], gu[0], gu[1], gs, out=h, static_weights=True)
+            tl.linear(h, dn[0], dn[1], gs, out=y_dn, static_weights=True)
+
+
 def capture(fn, stream):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -340,6 +389,26 @@ def main():
                          "eff_TFLOPs": round(flops(cfg, M) / (mt * 1e-3) / 1e12, 2)}
         del gm
 
+    # the same layers in the fused layout (QKV, o, gate/up + SiLU product, down)
+    fused = None
+    fs = FusedStack(stack)
+    if fs.ok:
+        fused = {"calls_per_layer": fs.calls_per_layer(),
+                 "layout": "QKV stacked; gate/up stacked with silu(gate)*up in its epilogue "
+                           "(ternary_linear_silu_mul); down reads that product",
+                 "per_M": {}}
+        for M in Ms:
+            reps = args.per_m_reps if args.per_m_reps > 0 else max(20, args.steps // 4)
+            gf = capture(lambda M=M: fs.run_m(tl, M), stream)
+            ft, _, _ = time_graph(gf, stream, reps, 3, lambda: None)
+            ft /= reps
+            fused["per_M"][str(M)] = {
+                "us_per_decode_step": round(ft * 1e3, 2),
+                "packed_GBps": round(packed_bytes(cfg) / (ft * 1e-3) / 1e9, 1),
+                "packed_frac_of_hbm": round(packed_bytes(cfg) / (ft * 1e-3) / 1e9 / peak, 4)}
+            del gf
+        del fs
+
     # end to end: pinned host x -> device, the calls, device out -> pinned host
     # (one copy per M pass in each direction: every call's x / out is a slice)
     e2e = None
@@ -388,7 +457,7 @@ def main():
                    "packed_bytes_per_step": pb, "algorithmic_bytes_per_step": ab,
                    "l2": "inputs larger than L2: distinct per-layer weights, "
                          f"{packed_bytes(cfg) / 1e9:.2f} GB packed per M pass",
-                   "per_M": per_m, "peaks_source": pk_src},
+                   "per_M": per_m, "fused_layout": fused, "peaks_source": pk_src},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "ternary_linear kernels (every launch of the step)",

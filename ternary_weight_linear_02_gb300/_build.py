@@ -47,9 +47,12 @@ def _fingerprint() -> str:
     h = hashlib.sha256()
     for f in _sources() + _headers():
         with open(f, "rb") as fh:
-            h.update(f.encode())
+            # the file name, not its absolute path: the same sources give the
+            # same fingerprint wherever the tree is checked out
+            h.update(os.path.basename(f).encode())
             h.update(fh.read())
-    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    flags = [os.path.basename(f) if f in (INCLUDE, CSRC) else f for f in ARCH + NVCC_FLAGS]
+    h.update(" ".join(flags).encode())
     return h.hexdigest()
 
 
