@@ -13,7 +13,7 @@ Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 (the layer shards across GPUs only as independent replicas here; no
 collective is on the data path): value = sum of ranks' work / max rank time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload cfg2]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode7b]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 """
 from __future__ import annotations
@@ -291,7 +291,7 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="cfg2", choices=sorted(CONFIGS))
+    ap.add_argument("--workload", default="decode7b", choices=sorted(CONFIGS))
     ap.add_argument("--ms", default="", help="comma list restricting M values")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of CPU oracle work for cpu_baseline")

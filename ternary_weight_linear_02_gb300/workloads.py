@@ -3,21 +3,21 @@
 No checkpoint is available; each config fixes only shapes, dtypes, the scale
 mode and the input distributions (see ``synth``):
 
-1. one linear, M=1, N=K=1024, fp16 x, per-128-group scales U[0.01,0.05]
+``linear1k``: one linear, M=1, N=K=1024, fp16 x, per-128-group scales U[0.01,0.05]
    (the ~0.6B embedding model of "三元量化模型接入vLLM：从逆向加载到Kernel优化的完整实战").
-2. 7B-shaped decode set: (N,K) = (4096,4096) q/k/v/o, (11008,4096) gate/up,
+``decode7b``: 7B-shaped decode set: (N,K) = (4096,4096) q/k/v/o, (11008,4096) gate/up,
    (4096,11008) down; M in {1,4,8,16}; bf16 x; per-channel scales
    U[0.005,0.05] (the Qwen2.5-7B ternary-in-vLLM write-up, §1.1, §1.3).
    As a decode step it runs through a 32-layer stack (a 7B model's depth),
    every layer with its own weights, so each step streams 1.62 GB of packed
    weights -- far more than the 129 MB L2.
-3. ~0.6B embedding model: hidden 1024, intermediate 3072, 28 layers of
+``embed06b``: ~0.6B embedding model: hidden 1024, intermediate 3072, 28 layers of
    q/k/v/o (1024x1024), gate/up (3072x1024), down (1024x3072); M in
    {64,256,1024}; fp16 x; per-128-group scales U[0.005,0.05]; about 0.1% of
    bytes carry one reserved 11 field.
-4. 27B-class layers: (5120,5120), (17408,5120), (5120,17408); M in {1,8,32};
+``layers27b``: 27B-class layers: (5120,5120), (17408,5120), (5120,17408); M in {1,8,32};
    bf16 x; per-128-group scales U[0.005,0.05].
-5. 7B-shaped decode / prefill stack: 28 layers of fused QKV (N=3584+512+512,
+``stack7b``: 7B-shaped decode / prefill stack: 28 layers of fused QKV (N=3584+512+512,
    K=3584), o (3584x3584), fused gate/up (N=2*18944, K=3584), down
    (N=3584, K=18944); M in {1,16,64,256,2048}; bf16 x; per-channel scales
    U[0.005,0.05].
@@ -52,26 +52,31 @@ class Config:
 
 
 CONFIGS = {
-    "cfg1": Config("cfg1", "single ternary linear M=1 K=N=1024 fp16 g128",
-                   (Layer("linear", 1024, 1024),), 1, (1,), torch.float16, 128, 0.01, 0.05),
-    "cfg2": Config("cfg2", "7B-shaped decode set (4096/11008), per-channel, bf16",
-                   (Layer("q", 4096, 4096), Layer("k", 4096, 4096), Layer("v", 4096, 4096),
-                    Layer("o", 4096, 4096), Layer("gate", 11008, 4096),
-                    Layer("up", 11008, 4096), Layer("down", 4096, 11008)),
-                   32, (1, 4, 8, 16), torch.bfloat16, 0, 0.005, 0.05),
-    "cfg3": Config("cfg3", "0.6B embedding model batch, 28 layers, fp16 g128, reserved codes",
-                   (Layer("q", 1024, 1024), Layer("k", 1024, 1024), Layer("v", 1024, 1024),
-                    Layer("o", 1024, 1024), Layer("gate", 3072, 1024), Layer("up", 3072, 1024),
-                    Layer("down", 1024, 3072)),
-                   28, (64, 256, 1024), torch.float16, 128, 0.005, 0.05, 0.001),
-    "cfg4": Config("cfg4", "27B-class layers (5120/17408), bf16 g128",
-                   (Layer("attn", 5120, 5120), Layer("up", 17408, 5120),
-                    Layer("down", 5120, 17408)),
-                   1, (1, 8, 32), torch.bfloat16, 128, 0.005, 0.05),
-    "cfg5": Config("cfg5", "7B-shaped 28-layer stack, fused QKV and gate/up, per-channel, bf16",
-                   (Layer("qkv", 4608, 3584, (3584, 512, 512)), Layer("o", 3584, 3584),
-                    Layer("gate_up", 37888, 3584, (18944, 18944)), Layer("down", 3584, 18944)),
-                   28, (1, 16, 64, 256, 2048), torch.bfloat16, 0, 0.005, 0.05),
+    "linear1k": Config(
+        "linear1k", "single ternary linear M=1 K=N=1024 fp16 g128",
+        (Layer("linear", 1024, 1024),), 1, (1,), torch.float16, 128, 0.01, 0.05),
+    "decode7b": Config(
+        "decode7b", "7B-shaped decode set (4096/11008), per-channel, bf16",
+        (Layer("q", 4096, 4096), Layer("k", 4096, 4096), Layer("v", 4096, 4096),
+         Layer("o", 4096, 4096), Layer("gate", 11008, 4096),
+         Layer("up", 11008, 4096), Layer("down", 4096, 11008)),
+        32, (1, 4, 8, 16), torch.bfloat16, 0, 0.005, 0.05),
+    "embed06b": Config(
+        "embed06b", "0.6B embedding model batch, 28 layers, fp16 g128, reserved codes",
+        (Layer("q", 1024, 1024), Layer("k", 1024, 1024), Layer("v", 1024, 1024),
+         Layer("o", 1024, 1024), Layer("gate", 3072, 1024), Layer("up", 3072, 1024),
+         Layer("down", 1024, 3072)),
+        28, (64, 256, 1024), torch.float16, 128, 0.005, 0.05, 0.001),
+    "layers27b": Config(
+        "layers27b", "27B-class layers (5120/17408), bf16 g128",
+        (Layer("attn", 5120, 5120), Layer("up", 17408, 5120),
+         Layer("down", 5120, 17408)),
+        1, (1, 8, 32), torch.bfloat16, 128, 0.005, 0.05),
+    "stack7b": Config(
+        "stack7b", "7B-shaped 28-layer stack, fused QKV and gate/up, per-channel, bf16",
+        (Layer("qkv", 4608, 3584, (3584, 512, 512)), Layer("o", 3584, 3584),
+         Layer("gate_up", 37888, 3584, (18944, 18944)), Layer("down", 3584, 18944)),
+        28, (1, 16, 64, 256, 2048), torch.bfloat16, 0, 0.005, 0.05),
 }
 
 

@@ -9,8 +9,8 @@ from ternary_weight_linear_02_gb300.workloads import (CONFIGS, algorithmic_bytes
                                                       packed_bytes, scale_bytes)
 
 
-def test_cfg2_byte_counts():
-    cfg = CONFIGS["cfg2"]
+def test_decode7b_byte_counts():
+    cfg = CONFIGS["decode7b"]
     per_layer = 4 * 4096 * 4096 // 4 + 2 * 11008 * 4096 // 4 + 4096 * 11008 // 4
     assert packed_bytes(cfg) == 32 * per_layer
     assert scale_bytes(cfg) == 32 * 2 * (4 * 4096 + 2 * 11008 + 4096)
@@ -38,7 +38,7 @@ class _RecordingTL:
 
 
 def test_fused_layout_reuses_the_same_weights():
-    cfg = dataclasses.replace(CONFIGS["cfg2"], depth=2)
+    cfg = dataclasses.replace(CONFIGS["decode7b"], depth=2)
     st = bench.Stack(cfg, (2,), torch.device("cpu"))
     fs = bench.FusedStack(st)
     assert fs.ok and fs.calls_per_layer() == 4
@@ -59,6 +59,6 @@ def test_fused_layout_reuses_the_same_weights():
 
 
 def test_fused_layout_needs_all_projections():
-    cfg = dataclasses.replace(CONFIGS["cfg4"], depth=1)
+    cfg = dataclasses.replace(CONFIGS["layers27b"], depth=1)
     st = bench.Stack(cfg, (1,), torch.device("cpu"))
     assert not bench.FusedStack(st).ok

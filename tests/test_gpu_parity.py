@@ -368,24 +368,24 @@ def test_linear_silu_mul(M, N, K, xdt, odt, gs):
     assert tl.device_status() == 0
 
 
-@pytest.mark.parametrize("M", [m for m in CONFIGS["cfg5"].Ms], ids=lambda m: f"cfg5-gate_up-M{m}")
+@pytest.mark.parametrize("M", [m for m in CONFIGS["stack7b"].Ms], ids=lambda m: f"stack7b-gate_up-M{m}")
 def test_silu_mul_full_size_sampled(M):
     """The 7B gate/up layer (2 x 18944 rows, K = 3584) at every M of the stack:
     decode kernel for M <= 32, tile kernel above; output column j needs only
     rows j and 18944 + j, so the oracle runs on sampled pairs."""
-    cfg = CONFIGS["cfg5"]
+    cfg = CONFIGS["stack7b"]
     layer = [l for l in cfg.layers if l.name == "gate_up"][0]
     n = layer.N // 2
     x, p, s = synth.layer(M, layer.N, layer.K, cfg.x_dtype, cfg.group_size, cfg.s_lo, cfg.s_hi,
-                          ("cfg5", "gate_up_silu", 0), DEV, cfg.p_reserved)
+                          ("stack7b", "gate_up_silu", 0), DEV, cfg.p_reserved)
     h = tl.linear_silu_mul(x, p, s, cfg.group_size, out_dtype=torch.float32)
     torch.cuda.synchronize()
-    J = sampled_rows(n, synth.seed_for("cfg5", "silu", M) & 0xFFFF, k=24)
+    J = sampled_rows(n, synth.seed_for("stack7b", "silu", M) & 0xFFFF, k=24)
     idx = torch.as_tensor(np.concatenate([J, n + J]), device=DEV)
     ps, ss = p[idx].contiguous(), s[idx].contiguous()
     h_ref, g_ref, u_ref = silu_refs(x, ps, ss, cfg.group_size)
     check_silu(h[:, torch.as_tensor(J, device=DEV)], h_ref, g_ref, u_ref, x, ss,
-               what=f"cfg5 gate_up silu M={M}")
+               what=f"stack7b gate_up silu M={M}")
     assert tl.device_status() == 0
 
 
