@@ -47,7 +47,6 @@ int skinny_max_m() {
 //   TERNARY_PDL_TRIGGER=1  release dependents after the main loop instead of at entry
 //                      =2  no explicit release (dependents start when the grid exits)
 //   TERNARY_SKINNY_SK=n    force the skinny path's K split (cluster size), 0 = automatic
-//   TERNARY_L2_PREFETCH=0  no L2 bulk prefetch before griddepcontrol.wait
 //   TERNARY_SKINNY_CTAS_PER_SM=n  CTAs per SM the tensor-core skinny path aims for (default 2)
 bool pdl_enabled() {
     static const bool v = env_int("TERNARY_PDL", 1) != 0;
@@ -57,8 +56,7 @@ bool pdl_enabled() {
 int skinny_launch_flags(uint32_t api_flags) {
     static const int trig = env_int("TERNARY_PDL_TRIGGER", 0);
     static const int base = (trig == 1 ? tl::kSkinnyTriggerLate : 0) |
-                            (trig == 2 ? tl::kSkinnyTriggerNever : 0) |
-                            (env_int("TERNARY_L2_PREFETCH", 1) ? tl::kSkinnyPrefetchL2 : 0);
+                            (trig == 2 ? tl::kSkinnyTriggerNever : 0);
     return base | ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kSkinnyStaticWeights : 0);
 }
 

@@ -23,7 +23,6 @@ constexpr int64_t kSkinnyTargetSmem = 100 * 1024;  // two CTAs per SM (overlap o
 // SkinnyArgs::flags
 constexpr int kSkinnyStaticWeights = 1;  // packed/scale may be read before griddepcontrol.wait
 constexpr int kSkinnyTriggerLate = 2;    // launch dependents after the main loop, not at entry
-constexpr int kSkinnyPrefetchL2 = 4;     // bulk-prefetch the CTA's packed rows into L2 at entry
 constexpr int kSkinnyTriggerNever = 8;   // no explicit trigger (dependents start at exit)
 
 struct SkinnyArgs {
