@@ -1,24 +1,27 @@
 #!/usr/bin/env python3
 """Benchmark of the ternary-weight linear layer on GB300.
 
-Default workload: the 7B-shaped decode set (N,K) in {(4096,4096) q/k/v/o,
-(11008,4096) gate/up, (4096,11008) down}, bf16 x, per-channel fp16 scales,
-M in {1,4,8,16}, run as decode steps through a 32-layer stack whose every
-layer has its own weights (1.62 GB of packed weights per M, far above the
-129 MB L2, so no flush is needed).  One bench step = one decode pass at each
-M (4 x 224 = 896 ternary_linear calls), captured once as a CUDA graph and
-replayed.
+Default workload (``stack7b``): the 7B-shaped 28-layer stack in the fused
+layout -- per model layer one fused QKV call (N = 3584 + 512 + 512, K = 3584),
+o (3584 x 3584), the fused gate/up call (2 x 18944 rows, K = 3584) with the
+SiLU-gated product in its epilogue, and down (3584 x 18944) reading that
+product -- bf16 x, per-channel fp16 scales.  One bench step is one pass of the
+stack at every M in {1, 16, 64, 256, 2048} (5 x 112 calls), each pass captured
+as a CUDA graph and replayed; the stack's per-layer weights are distinct
+(1.63 GB packed per pass, far above the 129 MB L2, so no flush is needed).
+The other four workloads are timed after the step and reported per M in
+``config.configs``.
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
-(the layer shards across GPUs only as independent replicas here; no
-collective is on the data path): value = sum of ranks' work / max rank time.
+(no collective on the data path): value = sum of ranks' work / max rank time.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode7b]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload stack7b]
   python bench.py --impl reference ...   # the CPU oracle on a bounded sample
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -34,10 +37,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from ternary_weight_linear_02_gb300 import dist_util, synth  # noqa: E402
-from ternary_weight_linear_02_gb300.workloads import CONFIGS, algorithmic_bytes, flops, packed_bytes  # noqa: E402
+from ternary_weight_linear_02_gb300.workloads import (CONFIGS, algorithmic_bytes, flops,  # noqa: E402
+                                                      layer_calls, out_cols, packed_bytes)
 
 METRIC = "packed-weight HBM GB/s and % of roofline per ternary_linear; µs/decode-step"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SUB_CONFIGS = ("linear1k", "decode7b", "embed06b", "layers27b")
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -113,14 +118,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def bench_config(key: str, depth: int = 0):
+    """The config as benchmarked: its depth times its weight rotation (so one
+    pass streams more than twice the L2), or an explicit depth."""
+    cfg = CONFIGS[key]
+    return dataclasses.replace(cfg, depth=depth if depth > 0 else cfg.depth * cfg.rotate)
+
+
 # ----------------------------------------------------------------------------- workload
-class Stack:
+class Workload:
     """Device-resident inputs of one config: per model layer, per projection,
-    packed weights and scales; per M, x and out buffers for every call."""
+    packed weights and scales; per M, every call's input and output buffer.
+    The independent inputs of one M pass are slices of one flat buffer and so are
+    the outputs, so an end-to-end step moves them in one copy each way."""
 
     def __init__(self, cfg, Ms, dev):
-        self.cfg, self.Ms, self.dev = cfg, Ms, dev
-        self.w = []  # [depth][proj] -> (packed, scale)
+        self.cfg, self.Ms, self.dev = cfg, tuple(Ms), dev
+        self.calls = layer_calls(cfg)
+        self.w = []  # [depth][layer] -> (packed, scale)
         for d in range(cfg.depth):
             row = []
             for l in cfg.layers:
@@ -131,89 +146,47 @@ class Stack:
                                      synth.seed_for(cfg.key, d, l.name, "s"), dev)
                 row.append((packed, scale))
             self.w.append(row)
-        # per M: every call's x and out are slices of one flat buffer, so an
-        # end-to-end step moves all of a pass's inputs / outputs in one copy each
-        self.x, self.out, self.xflat, self.oflat = {}, {}, {}, {}
-        for M in Ms:
-            nx = sum(M * l.K for l in cfg.layers) * cfg.depth
-            no = sum(M * l.N for l in cfg.layers) * cfg.depth
+        self.xflat, self.oflat, self.x, self.y = {}, {}, {}, {}
+        for M in self.Ms:
+            nx = cfg.depth * sum(M * cfg.layers[c.layer].K for c in self.calls if c.src < 0)
+            no = cfg.depth * sum(M * out_cols(cfg, c) for c in self.calls)
             self.xflat[M] = torch.empty(nx, dtype=cfg.x_dtype, device=dev)
             self.oflat[M] = torch.empty(no, dtype=cfg.x_dtype, device=dev)
-            xs, outs, ox, oo = [], [], 0, 0
+            xs, ys, ox, oo = [], [], 0, 0
             for d in range(cfg.depth):
-                xr, orow = [], []
-                for l in cfg.layers:
-                    xv = self.xflat[M][ox:ox + M * l.K].view(M, l.K)
-                    xv.copy_(synth.activations(M, l.K, cfg.x_dtype,
-                                               synth.seed_for(cfg.key, d, l.name, "x", M), dev))
-                    xr.append(xv)
-                    orow.append(self.oflat[M][oo:oo + M * l.N].view(M, l.N))
-                    ox += M * l.K
-                    oo += M * l.N
+                xr, yr = [], []
+                for j, c in enumerate(self.calls):
+                    l = cfg.layers[c.layer]
+                    n = out_cols(cfg, c)
+                    yr.append(self.oflat[M][oo:oo + M * n].view(M, n))
+                    oo += M * n
+                    if c.src < 0:
+                        xv = self.xflat[M][ox:ox + M * l.K].view(M, l.K)
+                        xv.copy_(synth.activations(M, l.K, cfg.x_dtype,
+                                                   synth.seed_for(cfg.key, d, l.name, j, "x", M), dev))
+                        ox += M * l.K
+                        xr.append(xv)
+                    else:
+                        xr.append(yr[c.src])
                 xs.append(xr)
-                outs.append(orow)
-            self.x[M], self.out[M] = xs, outs
+                ys.append(yr)
+            self.x[M], self.y[M] = xs, ys
 
-    def calls_per_step(self):
-        return len(self.Ms) * self.cfg.depth * len(self.cfg.layers)
-
-    def run_step(self, tl):
+    def run(self, tl, M):
+        """One pass of the stack at M tokens (every call with static weights)."""
         cfg = self.cfg
-        for M in self.Ms:
-            for d in range(cfg.depth):
-                for j, l in enumerate(cfg.layers):
-                    packed, scale = self.w[d][j]
+        for d in range(cfg.depth):
+            for j, c in enumerate(self.calls):
+                packed, scale = self.w[d][c.layer]
+                if c.kind == "silu_mul":
+                    tl.linear_silu_mul(self.x[M][d][j], packed, scale, cfg.group_size,
+                                       out=self.y[M][d][j], static_weights=True)
+                else:
                     tl.linear(self.x[M][d][j], packed, scale, cfg.group_size,
-                              out=self.out[M][d][j], static_weights=True)
+                              out=self.y[M][d][j], static_weights=True)
 
-
-class FusedStack:
-    """The same weights in the fused layout a vLLM-style model runs: per layer
-    one QKV call (q, k, v rows stacked), o, one gate/up call with the SiLU-gated
-    product in its epilogue (ternary_linear_silu_mul), and down reading that
-    product -- 4 calls per layer instead of 7, the same packed bytes."""
-
-    NAMES = ("q", "k", "v", "o", "gate", "up", "down")
-
-    def __init__(self, stack):
-        cfg = stack.cfg
-        names = [l.name for l in cfg.layers]
-        self.ok = all(n in names for n in self.NAMES)
-        if not self.ok:
-            return
-        ix = {n: i for i, n in enumerate(names)}
-        self.cfg, self.stack = cfg, stack
-        self.w = []
-        for d in range(cfg.depth):
-            w = stack.w[d]
-            qkv = tuple(torch.cat([w[ix[n]][t] for n in "qkv"]) for t in (0, 1))
-            gu = tuple(torch.cat([w[ix["gate"]][t], w[ix["up"]][t]]) for t in (0, 1))
-            self.w.append((qkv, w[ix["o"]], gu, w[ix["down"]]))
-        self.ix = ix
-        self.bufs = {}
-        for M in stack.Ms:
-            layer = []
-            for d in range(cfg.depth):
-                qkv_n = self.w[d][0][0].shape[0]
-                o_n = self.w[d][1][0].shape[0]
-                h_n = self.w[d][2][0].shape[0] // 2
-                dn_n = self.w[d][3][0].shape[0]
-                layer.append(tuple(torch.empty((M, n), dtype=cfg.x_dtype, device=stack.dev)
-                                   for n in (qkv_n, o_n, h_n, dn_n)))
-            self.bufs[M] = layer
-
-    def calls_per_layer(self):
-        return 4
-
-    def run_m(self, tl, M):
-        cfg, st, ix = self.cfg, self.stack, self.ix
-        for d in range(cfg.depth):
-            (qkv, o, gu, dn), (y_qkv, y_o, h, y_dn) = self.w[d], self.bufs[M][d]
-            gs = cfg.group_size
-            tl.linear(st.x[M][d][ix["q"]], qkv[0], qkv[1], gs, out=y_qkv, static_weights=True)
-            tl.linear(st.x[M][d][ix["o"]], o[0], o[1], gs, out=y_o, static_weights=True)
-            tl.linear_silu_mul(st.x[M][d][ix["gate"]], gu[0], gu[1], gs, out=h, static_weights=True)
-            tl.linear(h, dn[0], dn[1], gs, out=y_dn, static_weights=True)
+    def calls_per_pass(self):
+        return self.cfg.depth * len(self.calls)
 
 
 def capture(fn, stream):
@@ -224,98 +197,263 @@ def capture(fn, stream):
     return g
 
 
-def time_graph(g, stream, steps, warmup, barrier):
+def time_passes(graphs, stream, steps, warmup, barrier):
+    """Replay the graphs in order `steps` times; CUDA events between graphs on the
+    launching stream.  Returns (total ms, per-graph ms, wall t0, wall t1)."""
     with torch.cuda.stream(stream):
         for _ in range(warmup):
-            g.replay()
+            for g in graphs:
+                g.replay()
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+          for _ in range(steps)]
     t0 = time.time()
     with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(steps):
-            g.replay()
-        e1.record(stream)
+        for s in range(steps):
+            ev[s][0].record(stream)
+            for i, g in enumerate(graphs):
+                g.replay()
+                ev[s][i + 1].record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     barrier()
-    return e0.elapsed_time(e1), t0, t1
+    per = [sum(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(steps)) for i in range(len(graphs))]
+    return sum(per), per, t0, t1
+
+
+def bound_of(M):
+    return "hbm" if M <= 32 else ("tensor" if M >= 256 else "hbm+tensor")
+
+
+def per_m_entry(cfg, M, ms, pk, calls):
+    """Per-M figures of one pass that took `ms` milliseconds."""
+    t = ms * 1e-3
+    ab = algorithmic_bytes(cfg, M)
+    fl = flops(cfg, M)
+    e = {"us_per_pass": round(ms * 1e3, 2), "us_per_call": round(ms * 1e3 / calls, 3),
+         "packed_GBps": round(packed_bytes(cfg) / t / 1e9, 1),
+         "algorithmic_GBps": round(ab / t / 1e9, 1),
+         "frac_of_hbm": round(ab / t / 1e9 / pk["hbm_gbs"], 4),
+         "eff_TFLOPs": round(fl / t / 1e12, 2),
+         "frac_of_bf16_burst": round(fl / t / 1e12 / pk["bf16_tflops"], 4),
+         "frac_of_bf16_sustained": round(fl / t / 1e12 / pk["bf16_tflops_sustained"], 4),
+         "bound": bound_of(M)}
+    return e
+
+
+def roofline_of(cfg, M, ms, pk, pk_src, traffic):
+    """The roofline object for the pass at M: every launch of one pass is the same
+    kernel family, so per-launch work / average launch time = pass work / pass time."""
+    t = ms * 1e-3
+    calls = cfg.depth * len(layer_calls(cfg))
+    if bound_of(M) == "tensor":
+        ach = flops(cfg, M) / t / 1e12
+        peak = pk["bf16_tflops"]
+        return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic, "M": M,
+                "kernel": f"tile kernel, every launch of the M={M} pass ({calls} launches)",
+                "peak_note": f"bf16_tflops (burst) of {pk_src} peaks; "
+                             f"{ach / pk['bf16_tflops_sustained']:.3f} of the sustained figure"}
+    ach = algorithmic_bytes(cfg, M) / t / 1e9
+    peak = pk["hbm_gbs"]
+    return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
+            "traffic": traffic, "M": M,
+            "kernel": f"decode kernel, every launch of the M={M} pass ({calls} launches)",
+            "peak_note": f"hbm_gbs of {pk_src} peaks"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(cfg, Ms, budget_s: float, threads: int):
-    """Time the CPU oracle, as it stands, on a bounded sample of the workload:
-    for every distinct (N, K) projection shape and every M, the first R output
-    rows (R = min(N, 256)), cycled until about budget_s seconds of work.
-    Returns (packed-weight GB/s of the sample, description, seconds)."""
+    """Time the CPU oracle, as it stands, on a bounded sample of the workload: for
+    every call of one model layer and every M, the first R output rows
+    (R = 256 for M <= 16, fewer for larger M so the sample stays bounded), cycled
+    until about budget_s seconds of work.  Returns (estimated packed-weight GB/s of
+    the whole pass set, description, seconds): the sampled time per row is scaled
+    to every row of every layer of the stack."""
     import oracle
     oracle.build()
-    shapes = []
-    for l in cfg.layers:
-        if (l.N, l.K) not in [(a, b) for a, b, _ in shapes]:
-            shapes.append((l.N, l.K, l.name))
     name = "f16" if cfg.x_dtype == torch.float16 else "bf16"
     items = []
-    for N, K, lname in shapes:
-        rows = min(N, 256)
-        p = synth.packed_codes(rows, K, synth.seed_for("cpu", N, K), "cpu").numpy()
-        groups = 0 if cfg.group_size == 0 else K // cfg.group_size
-        s = synth.scales(rows, groups, cfg.s_lo, cfg.s_hi, 1, "cpu")
-        sb = s.view(torch.int16).numpy().view(np.uint16)
+    for j, c in enumerate(layer_calls(cfg)):
+        l = cfg.layers[c.layer]
         for M in Ms:
-            x = synth.activations(M, K, cfg.x_dtype, synth.seed_for("cpu", K, M), "cpu")
+            rows = min(l.N, max(8, 256 * 16 // max(M, 16)))
+            if c.kind == "silu_mul":  # rows pairs: gate rows then the matching up rows
+                rows = 2 * min(l.N // 2, max(4, rows // 2))
+            p = synth.packed_codes(rows, l.K, synth.seed_for("cpu", l.name, l.K), "cpu").numpy()
+            groups = 0 if cfg.group_size == 0 else l.K // cfg.group_size
+            s = synth.scales(rows, groups, cfg.s_lo, cfg.s_hi, 1, "cpu")
+            sb = s.view(torch.int16).numpy().view(np.uint16)
+            x = synth.activations(M, l.K, cfg.x_dtype, synth.seed_for("cpu", l.K, M), "cpu")
             xb = x.contiguous().view(torch.int16).numpy().view(np.uint16)
-            items.append((xb, p, sb, rows * K // 4, f"{N}x{K}@M{M}[{rows} rows]"))
-    done_bytes, spent, passes = 0, 0.0, 0
-    while spent < budget_s or passes == 0:
-        for xb, p, sb, nbytes, _ in items:
+            # share of the call this sample stands for: weight rows sampled / rows of the call
+            frac = rows / l.N
+            items.append((c.kind, xb, p, sb, frac, l, M, f"{l.name}@M{M}[{rows} rows]"))
+    spent = {i: 0.0 for i in range(len(items))}
+    runs = {i: 0 for i in range(len(items))}
+    total, passes = 0.0, 0
+    while total < budget_s or passes == 0:
+        for i, (kind, xb, p, sb, frac, l, M, _) in enumerate(items):
             t0 = time.perf_counter()
-            oracle.linear_from_bits(xb, name, p, sb, cfg.group_size, threads)
-            spent += time.perf_counter() - t0
-            done_bytes += nbytes
+            if kind == "silu_mul":
+                oracle.silu_mul_from_bits(xb, name, p, sb, cfg.group_size, threads)
+            else:
+                oracle.linear_from_bits(xb, name, p, sb, cfg.group_size, threads)
+            dt = time.perf_counter() - t0
+            spent[i] += dt
+            runs[i] += 1
+            total += dt
         passes += 1
-    gbs = done_bytes / spent / 1e9
-    desc = (f"oracle fp64 C with {threads} threads on {len(items)} slices of {cfg.key} "
-            f"({', '.join(i[4] for i in items)}), {passes} passes, {spent:.1f} s of CPU work; "
-            "value = packed bytes of the slices / CPU time")
-    return gbs, desc, spent
+    # estimated CPU seconds of one pass at each M = depth * sum over calls (time / frac)
+    est = 0.0
+    for i, (_, _, _, _, frac, _, _, _) in enumerate(items):
+        est += cfg.depth * (spent[i] / runs[i]) / frac
+    gbs = packed_bytes(cfg) * len(Ms) / est / 1e9
+    desc = (f"oracle fp64 C with {threads} thread(s) on {len(items)} row slices of {cfg.key} "
+            f"({', '.join(i[7] for i in items)}), {passes} passes, {total:.1f} s of CPU work; "
+            f"per-row time scaled to the full {cfg.depth}-layer pass at each M "
+            "(extrapolated); value = packed bytes of the step / estimated CPU time")
+    return gbs, desc, total
+
+
+# ----------------------------------------------------------------------------- comparators
+def time_comparators(wl, tl, stream, reps):
+    """The same stack and inputs on the pages' route 1, with cuBLAS (torch.matmul)
+    doing the product: (a) weights dequantised once to the activation dtype at load
+    (t * scale), (b) dequantised on the fly every call (ternary_unpack, then t * scale
+    in torch, then the matmul).  The gated gate/up call forms silu(g) * u with torch
+    after its matmul.  Reported as the same packed-weight GB/s for comparison."""
+    cfg = wl.cfg
+    dt = cfg.x_dtype
+
+    def dequant(packed, scale, l):
+        t, _ = tl.unpack(packed)
+        if cfg.group_size == 0:
+            w = t.to(torch.float32) * scale.to(torch.float32)[:, None]
+        else:
+            w = (t.to(torch.float32).view(l.N, -1, cfg.group_size)
+                 * scale.to(torch.float32)[:, :, None]).view(l.N, l.K)
+        return w.to(dt)
+
+    def product(x, w, c, out):
+        if c.kind == "silu_mul":
+            y = torch.matmul(x, w.t())
+            n = y.shape[1] // 2
+            torch.mul(torch.nn.functional.silu(y[:, :n]), y[:, n:], out=out)
+        else:
+            torch.matmul(x, w.t(), out=out)
+
+    res = {}
+    # (a) dequantise once at load
+    W = [[dequant(p, s, cfg.layers[i]) for i, (p, s) in enumerate(row)] for row in wl.w]
+    torch.cuda.synchronize()
+    per = {}
+    for M in wl.Ms:
+        def step(M=M):
+            for d in range(cfg.depth):
+                for j, c in enumerate(wl.calls):
+                    product(wl.x[M][d][j], W[d][c.layer], c, wl.y[M][d][j])
+        step()
+        g = capture(step, stream)
+        _, pm, _, _ = time_passes([g], stream, reps, 2, lambda: None)
+        per[str(M)] = per_m_brief(cfg, M, pm[0] / reps)
+        del g
+    res["dequant_at_load"] = {"kind": f"weights dequantised once to {dt_name(dt)} (t * scale), "
+                                      "torch.matmul (cuBLAS)", "per_M": per}
+    del W
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    # (b) dequantise on the fly, every call
+    per = {}
+    for M in wl.Ms:
+        def step(M=M):
+            for d in range(cfg.depth):
+                for j, c in enumerate(wl.calls):
+                    p, s = wl.w[d][c.layer]
+                    product(wl.x[M][d][j], dequant(p, s, cfg.layers[c.layer]), c, wl.y[M][d][j])
+        step()
+        g = capture(step, stream)
+        _, pm, _, _ = time_passes([g], stream, reps, 2, lambda: None)
+        per[str(M)] = per_m_brief(cfg, M, pm[0] / reps)
+        del g
+        torch.cuda.empty_cache()
+    res["dequant_on_the_fly"] = {"kind": "every call: ternary_unpack to int8, t * scale in torch to "
+                                         f"{dt_name(dt)}, torch.matmul (cuBLAS)", "per_M": per}
+    return res
+
+
+def per_m_brief(cfg, M, ms):
+    t = ms * 1e-3
+    return {"us_per_pass": round(ms * 1e3, 2), "packed_GBps": round(packed_bytes(cfg) / t / 1e9, 1),
+            "eff_TFLOPs": round(flops(cfg, M) / t / 1e12, 2)}
+
+
+def dt_name(dt):
+    return "bf16" if dt == torch.bfloat16 else "f16"
+
+
+def time_config(key, tl, stream, dev, reps, pk, pk_src):
+    """Compact per-M figures of one config (its own stack, rotated past the L2)."""
+    cfg = bench_config(key)
+    wl = Workload(cfg, cfg.Ms, dev)
+    for M in cfg.Ms:
+        wl.run(tl, M)
+    torch.cuda.synchronize()
+    graphs = [capture(lambda M=M: wl.run(tl, M), stream) for M in cfg.Ms]
+    _, per, _, _ = time_passes(graphs, stream, reps, 3, lambda: None)
+    calls = wl.calls_per_pass()
+    out = {"workload": describe(cfg, cfg.Ms), "calls_per_pass": calls, "reps": reps, "per_M": {}}
+    for M, ms in zip(cfg.Ms, per):
+        e = per_m_entry(cfg, M, ms / reps, pk, calls)
+        out["per_M"][str(M)] = e
+    del graphs, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
+def describe(cfg, Ms):
+    calls = layer_calls(cfg)
+    parts = []
+    for c in calls:
+        l = cfg.layers[c.layer]
+        tag = "silu(gate)*up of " if c.kind == "silu_mul" else ""
+        src = f" <- call {c.src}" if c.src >= 0 else ""
+        parts.append(f"{tag}{l.name} {l.N}x{l.K}{src}")
+    return (f"{cfg.key}: {cfg.title}; {cfg.depth} model layers (distinct weights); per layer "
+            + ", ".join(parts) + f"; M in {list(Ms)}; {dt_name(cfg.x_dtype)} x; "
+            + ("per-channel" if cfg.group_size == 0 else f"group-{cfg.group_size}") + " fp16 scales")
 
 
 # ----------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode7b", choices=sorted(CONFIGS))
+    ap.add_argument("--workload", default="stack7b", choices=sorted(CONFIGS))
     ap.add_argument("--ms", default="", help="comma list restricting M values")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
-                    help="seconds of CPU oracle work for cpu_baseline")
+                    help="seconds of CPU oracle work for cpu_baseline (all threads)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other configs' figures")
+    ap.add_argument("--no-comparator", action="store_true", help="skip the cuBLAS comparators")
     ap.add_argument("--depth", type=int, default=0,
                     help="override the number of model layers (small cases for profiling)")
-    ap.add_argument("--per-m-reps", type=int, default=0,
-                    help="graph replays for each per-M timing (default: max(20, steps/4))")
-    ap.add_argument("--comparator", action="store_true",
-                    help="also time the same stack with weights dequantised once to bf16 "
-                         "(t * scale) and torch.matmul (cuBLAS)")
+    ap.add_argument("--reps", type=int, default=0,
+                    help="replays per pass for the other configs and comparators (default 10)")
     args = ap.parse_args()
 
     rank, world, local = dist_env()
-    cfg = CONFIGS[args.workload]
-    if args.depth > 0:
-        import dataclasses
-        cfg = dataclasses.replace(cfg, depth=args.depth)
+    cfg = bench_config(args.workload, args.depth)
     Ms = tuple(int(v) for v in args.ms.split(",")) if args.ms else cfg.Ms
     threads = os.cpu_count() or 1
-    workload_name = (f"{cfg.key}: {cfg.title}; depth {cfg.depth}; "
-                     + ", ".join(f"{l.name} {l.N}x{l.K}" for l in cfg.layers) + f"; M in {list(Ms)}")
-    xdt = "bf16" if cfg.x_dtype == torch.bfloat16 else "f16"
+    workload_name = describe(cfg, Ms)
+    pk, pk_src = peaks()
 
     if args.impl == "reference":
         if rank != 0:
@@ -328,7 +466,7 @@ def main():
             if i >= args.warmup:
                 vals.append((v, spent))
         value = statistics.median(v for v, _ in vals)
-        ms = statistics.median(s for _, s in vals) * 1e3
+        ms = packed_bytes(cfg) * len(Ms) / (value * 1e9) * 1e3
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -353,118 +491,108 @@ def main():
     tl.build()
     tl.load()
 
-    stack = Stack(cfg, Ms, dev)
+    wl = Workload(cfg, Ms, dev)
     torch.cuda.synchronize()
-    # first call on the device outside capture (creates the status word)
-    stack.run_step(tl)
+    for M in Ms:  # first calls on the device outside capture (create the status word)
+        wl.run(tl, M)
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream(dev)
     stream.wait_stream(torch.cuda.current_stream(dev))
-    g = capture(lambda: stack.run_step(tl), stream)
+    graphs = [capture(lambda M=M: wl.run(tl, M), stream) for M in Ms]
 
     clocks = ClockSampler(local)
     time.sleep(0.3)
-    ms_total, t0, t1 = time_graph(g, stream, args.steps, args.warmup, barrier)
+    ms_total, per_ms, t0, t1 = time_passes(graphs, stream, args.steps, args.warmup, barrier)
     clocks.window(t0, t1)
     clk = clocks.stop()
     ms_step = dist_util.max_over_ranks(ms_total / args.steps, dev)
 
     pb = packed_bytes(cfg) * len(Ms)
-    ab = sum(algorithmic_bytes(cfg, M) for M in Ms)
     value = dist_util.job_throughput(pb, ms_step, world) / 1e9
-    calls = stack.calls_per_step()
-    pk, pk_src = peaks()
-    peak = pk["hbm_gbs"]
-    achieved = ab / (ms_step * 1e-3) / 1e9  # every launch of the step is the linear kernel
-    per_m = {}
-    for M in Ms:  # per-M decode-step time: time one M pass alone
-        reps = args.per_m_reps if args.per_m_reps > 0 else max(20, args.steps // 4)
-        gm = capture(lambda M=M: Stack.run_step(_OneM(stack, M), tl), stream)
-        mt, _, _ = time_graph(gm, stream, reps, 3, lambda: None)
-        mt /= reps
-        per_m[str(M)] = {"us_per_decode_step": round(mt * 1e3, 2),
-                         "packed_GBps": round(packed_bytes(cfg) / (mt * 1e-3) / 1e9, 1),
-                         "frac_of_hbm": round(algorithmic_bytes(cfg, M) / (mt * 1e-3) / 1e9 / peak, 4),
-                         "eff_TFLOPs": round(flops(cfg, M) / (mt * 1e-3) / 1e12, 2)}
-        del gm
+    calls = wl.calls_per_pass()
+    per_m = {str(M): per_m_entry(cfg, M, ms / args.steps, pk, calls) for M, ms in zip(Ms, per_ms)}
+    traffic = read_traffic(cfg.key)
+    # the dominant kernel: the pass with the largest share of the step
+    dom = max(range(len(Ms)), key=lambda i: per_ms[i])
+    roofline = roofline_of(cfg, Ms[dom], per_ms[dom] / args.steps, pk, pk_src, traffic)
+    roofline["share_of_step"] = round(per_ms[dom] / ms_total, 4)
+    per_m_roof = {str(M): roofline_of(cfg, M, ms / args.steps, pk, pk_src, None)
+                  for M, ms in zip(Ms, per_ms)}
+    decode_us = {str(M): per_m[str(M)]["us_per_pass"] for M in Ms if M <= 32}
 
-    # the same layers in the fused layout (QKV, o, gate/up + SiLU product, down)
-    fused = None
-    fs = FusedStack(stack)
-    if fs.ok:
-        fused = {"calls_per_layer": fs.calls_per_layer(),
-                 "layout": "QKV stacked; gate/up stacked with silu(gate)*up in its epilogue "
-                           "(ternary_linear_silu_mul); down reads that product",
-                 "per_M": {}}
-        for M in Ms:
-            reps = args.per_m_reps if args.per_m_reps > 0 else max(20, args.steps // 4)
-            gf = capture(lambda M=M: fs.run_m(tl, M), stream)
-            ft, _, _ = time_graph(gf, stream, reps, 3, lambda: None)
-            ft /= reps
-            fused["per_M"][str(M)] = {
-                "us_per_decode_step": round(ft * 1e3, 2),
-                "packed_GBps": round(packed_bytes(cfg) / (ft * 1e-3) / 1e9, 1),
-                "packed_frac_of_hbm": round(packed_bytes(cfg) / (ft * 1e-3) / 1e9 / peak, 4)}
-            del gf
-        del fs
-
-    # end to end: pinned host x -> device, the calls, device out -> pinned host
-    # (one copy per M pass in each direction: every call's x / out is a slice)
+    # end to end: pinned host inputs -> device, the pass, device outputs -> pinned host
+    # (one copy each way per M pass: every call's own input / output is a slice)
     e2e = None
     if not args.no_e2e:
-        hx = {M: stack.xflat[M].cpu().pin_memory() for M in Ms}
-        ho = {M: torch.empty(stack.oflat[M].shape, dtype=cfg.x_dtype).pin_memory() for M in Ms}
+        hx = {M: wl.xflat[M].cpu().pin_memory() for M in Ms}
+        ho = {M: torch.empty(wl.oflat[M].shape, dtype=cfg.x_dtype).pin_memory() for M in Ms}
         h2d = sum(t.numel() * t.element_size() for t in hx.values())
         d2h = sum(t.numel() * t.element_size() for t in ho.values())
 
-        def e2e_step():
-            for M in Ms:
-                stack.xflat[M].copy_(hx[M], non_blocking=True)
-            stack.run_step(tl)
-            for M in Ms:
-                ho[M].copy_(stack.oflat[M], non_blocking=True)
+        def e2e_pass(M):
+            wl.xflat[M].copy_(hx[M], non_blocking=True)
+            wl.run(tl, M)
+            ho[M].copy_(wl.oflat[M], non_blocking=True)
 
-        ge = capture(e2e_step, stream)
-        e_ms, _, _ = time_graph(ge, stream, args.steps, args.warmup, barrier)
+        ge = [capture(lambda M=M: e2e_pass(M), stream) for M in Ms]
+        e_ms, _, _, _ = time_passes(ge, stream, args.steps, args.warmup, barrier)
         e_step = dist_util.max_over_ranks(e_ms / args.steps, dev)
         e2e = {"value": dist_util.job_throughput(pb, e_step, world) / 1e9, "unit": "GB/s",
-               "ms_per_step": e_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e_step, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "path": "ternary_weight_linear_02_gb300.linear / linear_silu_mul (C ABI through "
+                       "ctypes), pinned host inputs copied in and outputs copied out in the "
+                       "timed region"}
         del ge
 
+    reps = args.reps if args.reps > 0 else 10
     comparator = None
-    if args.comparator:
-        comparator = time_comparator(stack, tl, stream, Ms, args)
+    if not args.no_comparator and world == 1:
+        comparator = time_comparators(wl, tl, stream, max(3, reps // 2))
 
     # a kernel wait that gave up (bounded waits) leaves a non-zero status word:
     # the outputs of that call are not valid, so the line says so
     torch.cuda.synchronize()
     dev_status = tl.device_status(clear=True)
     if dev_status != 0:
-        print(f"bench: device status {tl.status_string(dev_status)} after the timed runs", file=sys.stderr)
+        print(f"bench: device status {tl.status_string(dev_status)} after the timed runs",
+              file=sys.stderr)
+    del graphs, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    configs = None
+    if not args.no_configs and args.workload == "stack7b" and not args.depth:
+        configs = {k: time_config(k, tl, stream, dev, reps, pk, pk_src) for k in SUB_CONFIGS}
+        st2 = tl.device_status(clear=True)
+        if st2 != 0:
+            print(f"bench: device status {tl.status_string(st2)} after the other configs",
+                  file=sys.stderr)
+            dev_status = dev_status or st2
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, desc, _ = oracle_sample(cfg, Ms, args.cpu_budget, threads)
-        cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+        v1, desc1, _ = oracle_sample(cfg, Ms, args.cpu_budget / 2, 1)
+        cpu = {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "single_thread": {"value": v1, "unit": "GB/s", "cores": 1, "sample": desc1}}
 
-    traffic = read_traffic(cfg.key)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": xdt, "data": "synthetic",
-        "config": {"workload": workload_name, "Ms": list(Ms), "calls_per_step": calls,
-                   "packed_bytes_per_step": pb, "algorithmic_bytes_per_step": ab,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt_name(cfg.x_dtype), "data": "synthetic",
+        "config": {"workload": workload_name, "Ms": list(Ms), "calls_per_step": calls * len(Ms),
+                   "packed_bytes_per_step": pb,
+                   "algorithmic_bytes_per_step": sum(algorithmic_bytes(cfg, M) for M in Ms),
                    "l2": "inputs larger than L2: distinct per-layer weights, "
-                         f"{packed_bytes(cfg) / 1e9:.2f} GB packed per M pass",
-                   "per_M": per_m, "fused_layout": fused, "peaks_source": pk_src},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "ternary_linear kernels (every launch of the step)",
-                     "peak_note": f"hbm_gbs of {pk_src} peaks"},
+                         f"{packed_bytes(cfg) / 1e9:.2f} GB packed per pass",
+                   "us_per_decode_step": decode_us,
+                   "per_M": per_m, "roofline_per_M": per_m_roof, "peaks_source": pk_src,
+                   "configs": configs},
+        "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": calls * args.steps,
+        "gpu_launches": calls * len(Ms) * args.steps,
         "comparator": comparator,
         "clocks": clk,
         "device_status": tl.status_string(dev_status),
@@ -477,65 +605,12 @@ def main():
     return 0
 
 
-def time_comparator(stack, tl, stream, Ms, args):
-    """The same decode stack with each layer's weights dequantised once to bf16
-    (t from ternary_unpack, times the scale) and run with torch.matmul (cuBLAS):
-    the dequantise-at-load route the pages compare against.  Reported as the same
-    packed-weight GB/s (packed bytes of the step / step time) for comparison."""
-    cfg = stack.cfg
-    W = []
-    for d in range(cfg.depth):
-        row = []
-        for j, l in enumerate(cfg.layers):
-            packed, scale = stack.w[d][j]
-            t, _ = tl.unpack(packed)
-            if cfg.group_size == 0:
-                w = t.to(torch.float32) * scale.to(torch.float32)[:, None]
-            else:
-                w = (t.to(torch.float32).view(l.N, -1, cfg.group_size)
-                     * scale.to(torch.float32)[:, :, None]).view(l.N, l.K)
-            row.append(w.to(cfg.x_dtype))
-            del t, w
-        W.append(row)
-    torch.cuda.synchronize()
-    res = {"kind": "weights dequantised once to " + ("bf16" if cfg.x_dtype == torch.bfloat16 else "fp16")
-           + " (t * scale) + torch.matmul (cuBLAS), same stack and inputs", "unit": "GB/s", "per_M": {}}
-    tot_ms = 0.0
-    for M in Ms:
-        def step(M=M):
-            for d in range(cfg.depth):
-                for j in range(len(cfg.layers)):
-                    torch.matmul(stack.x[M][d][j], W[d][j].t(), out=stack.out[M][d][j])
-        step()
-        g = capture(step, stream)
-        reps = args.per_m_reps if args.per_m_reps > 0 else max(20, args.steps // 4)
-        mt, _, _ = time_graph(g, stream, reps, 3, lambda: None)
-        mt /= reps
-        tot_ms += mt
-        res["per_M"][str(M)] = {"us_per_decode_step": round(mt * 1e3, 2),
-                                "packed_GBps": round(packed_bytes(cfg) / (mt * 1e-3) / 1e9, 1),
-                                "bf16_weight_GBps": round(packed_bytes(cfg) * 8 / (mt * 1e-3) / 1e9, 1)}
-        del g
-    res["value"] = packed_bytes(cfg) * len(Ms) / (tot_ms * 1e-3) / 1e9
-    del W
-    torch.cuda.empty_cache()
-    return res
-
-
-class _OneM:
-    """A view of a Stack restricted to one M (for the per-M timings)."""
-
-    def __init__(self, stack, M):
-        self.cfg, self.Ms, self.w, self.x, self.out = stack.cfg, (M,), stack.w, stack.x, stack.out
-
-
 def read_traffic(key):
     """Per-launch DRAM traffic from the committed ncu summary for this
     workload, if its kernel fingerprint matches the current sources."""
     path = os.path.join(ROOT, "profiles", f"traffic_{key}.txt")
     if not os.path.exists(path):
         return None
-    want = None
     vals = {}
     for line in open(path):
         if ":" in line and not line.startswith("#"):

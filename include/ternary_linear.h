@@ -94,9 +94,8 @@ tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
  *                       out[m,n] = sum_g scale[n,g] * sum_{k in group g} t[n,k] x[m,k]
  *                       ("三元量化模型接入vLLM…完整实战" §1.1, §3.1, §4.2)
  *   group_size == 64  : the same with 64-wide groups, scale fp16 [N, K/64]
- *                       ("Bonsai 2 27B" port §4.2, §5.2); served by the tile
- *                       kernel for every M (TL_PATH_SKINNY returns
- *                       TL_ERR_UNSUPPORTED for it)
+ *                       ("Bonsai 2 27B" port §4.2, §5.2); the skinny path
+ *                       serves it for M <= 16, the tile kernel above
  *   group_size == 256 : the same with 256-wide groups, scale fp16 [N, K/256]
  *                       (the coarser per-group choice of "第13章 量化：精度与速度的
  *                       工程平衡" §13.3.3); every path serves it
@@ -156,6 +155,10 @@ tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t 
                                   int32_t out_dtype, int64_t M, int64_t N, int64_t K,
                                   uint32_t flags, void *stream);
 
+/* Kernels by M (TL_PATH_AUTO): M <= 16 -> the decode kernel (register-fed warp
+ * MMAs, TMA-staged weights); 17 <= M <= 32 -> the tcgen05 skinny kernel (64-wide
+ * groups: tile kernel); larger M -> the tcgen05 tile kernel. */
+
 /* Largest M the automatic dispatch sends to the skinny path (default 32,
  * overridable with the environment variable TERNARY_SKINNY_MAX_M, read once). */
 int32_t ternary_skinny_max_m(void);
@@ -168,6 +171,18 @@ int32_t ternary_skinny_max_m(void);
  */
 tl_status ternary_device_status(int32_t *code, int32_t clear);
 
+/*
+ * ternary_device_status_async -- enqueue on `stream` a copy of the current
+ * device's status word into *dst (device memory or pinned host memory, 4-byte
+ * aligned; the raw word: 0 = OK, 7 = a bounded wait gave up), then, if clear is
+ * non-zero, reset the word.  The copy is ordered after the work already on
+ * `stream`, so a non-zero value read after synchronising `stream` was set by
+ * that work or by work on another stream that ran before it.  Asynchronous.
+ * Errors: TL_ERR_NULL (dst NULL), TL_ERR_ALIGN, TL_ERR_CUDA,
+ * TL_ERR_UNSUPPORTED (no sm_103 device).
+ */
+tl_status ternary_device_status_async(int32_t *dst, int32_t clear, void *stream);
+
 /* Human-readable name of a tl_status value (static storage, never NULL). */
 const char *ternary_status_string(int32_t status);
 
@@ -178,6 +193,16 @@ int32_t ternary_version(void);
  * return TL_ERR_CUDA without touching CUDA, as a failed launch would.  Lets
  * error handling above the ABI be exercised without a GPU fault. */
 void ternary_test_inject_launch_failures(int32_t n);
+
+/* Testing aid: the give-up time, in SM clock cycles, of the decode kernel's
+ * main-loop waits for every later launch (cycles <= 0 restores the default of
+ * about 2^30 cycles, ~0.5 s).  stall != 0 additionally makes each of those
+ * launches first wait on a barrier that nothing arrives on, so the wait runs
+ * out: the call then writes no output and sets the device status word to
+ * TL_ERR_TIMEOUT, while every copy in flight still lands before the kernel
+ * exits (those waits keep the default limit).  Lets the give-up path be tested
+ * without a fault or a hang. */
+void ternary_test_set_wait_limit(int64_t cycles, int32_t stall);
 
 #ifdef __cplusplus
 }

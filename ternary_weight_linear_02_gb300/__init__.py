@@ -20,7 +20,7 @@ import torch
 __all__ = [
     "TernaryError", "build", "library_path", "load", "pack", "unpack", "linear", "linear_fused",
     "linear_silu_mul",
-    "device_status", "status_string", "skinny_max_m", "PATHS",
+    "device_status", "device_status_async", "status_string", "skinny_max_m", "PATHS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -78,6 +78,10 @@ def load():
     lib.ternary_version.restype = i32
     lib.ternary_test_inject_launch_failures.argtypes = [i32]
     lib.ternary_test_inject_launch_failures.restype = None
+    lib.ternary_test_set_wait_limit.argtypes = [i64, i32]
+    lib.ternary_test_set_wait_limit.restype = None
+    lib.ternary_device_status_async.argtypes = [p, i32, p]
+    lib.ternary_device_status_async.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -210,6 +214,17 @@ def device_status(clear: bool = True) -> int:
     code = ctypes.c_int32(0)
     _check(load().ternary_device_status(ctypes.byref(code), int(clear)), "ternary_device_status")
     return int(code.value)
+
+
+def device_status_async(dst: torch.Tensor, clear: bool = True) -> torch.Tensor:
+    """Enqueue a copy of the status word into ``dst`` (an int32 tensor of one
+    element on the device, or pinned on the host) on the current stream."""
+    if dst.dtype != torch.int32 or dst.numel() != 1:
+        raise ValueError("dst must be a one-element int32 tensor")
+    dev = dst.device if dst.is_cuda else torch.device("cuda", torch.cuda.current_device())
+    _check(load().ternary_device_status_async(_ptr(dst), int(clear), _stream(dev)),
+           "ternary_device_status_async")
+    return dst
 
 
 def linear_silu_mul(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,

@@ -25,6 +25,9 @@ struct DevInfo {
 std::mutex g_mu;
 DevInfo g_dev[kMaxDevices];
 std::atomic<int> g_inject_launch_failures{0};
+// testing aids for the decode kernel's bounded waits (ternary_test_set_wait_limit)
+std::atomic<long long> g_wait_limit{0};  // 0 = the default (~0.5 s)
+std::atomic<int> g_stall{0};
 
 int env_int(const char *name, int dflt) {
     const char *v = std::getenv(name);
@@ -60,23 +63,30 @@ int skinny_launch_flags(uint32_t api_flags) {
     return base | ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kSkinnyStaticWeights : 0);
 }
 
-// Skinny-path kernel choice.  The tcgen05 kernel (decoded weights in TMEM, 128-row
-// tiles, cluster split-K) is faster from M = 3 tokens up; for M <= 2 the register-fed
-// mma.sync kernel (16-row CTAs, no split-K, a much shorter critical path per CTA)
-// measured faster on the 7B-shaped decode set.
-//   TERNARY_SKINNY_IMPL=tc | mma   force one of the two kernels for every M <= 32
-//   TERNARY_SKINNY_TC_MIN_M=n      smallest M sent to the tcgen05 kernel (default 3)
-bool skinny_impl_tc(int64_t M) {
+// Skinny-path kernel choice.  M <= 16: the decode kernel of gemv.cuh (register-fed
+// warp MMAs, TMA-staged weights, x fragments held in registers per 64-k column).
+// 17 <= M <= 32: the tcgen05 kernel (decoded weights in TMEM, 128-row tiles).
+//   TERNARY_SKINNY_IMPL=tc | mma   force the tcgen05 kernel, or the older warp-MMA
+//                                  kernel of kern_skinny.cu, for every M <= 32
+enum { kImplAuto = 0, kImplMma = 1, kImplTc = 2 };
+int skinny_impl() {
     static const int mode = [] {
         const char *e = std::getenv("TERNARY_SKINNY_IMPL");
-        if (e && e[0] == 'm') return 1;
-        if (e && e[0] == 't') return 2;
-        return 0;
+        if (e && e[0] == 'm') return (int)kImplMma;
+        if (e && e[0] == 't') return (int)kImplTc;
+        return (int)kImplAuto;
     }();
-    static const int min_m = env_int("TERNARY_SKINNY_TC_MIN_M", 3);
-    if (mode == 1) return false;
-    if (mode == 2) return true;
-    return M >= min_m;
+    return mode;
+}
+
+int gemv_flags(uint32_t api_flags) {
+    return ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kGemvStaticWeights : 0) |
+           (g_stall.load() ? tl::kGemvTestStall : 0);
+}
+
+long long wait_limit() {
+    const long long v = g_wait_limit.load();
+    return v > 0 ? v : (1ll << 30);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -187,25 +197,48 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
 
     const bool bf = x_dtype == TL_BF16;
     const bool group = group_size != 0;
-    // 64-wide groups are served by the tile kernel (it applies the scale per
-    // 64-k chunk); the skinny kernels fold scales per 128-k unit
     const bool g64 = group_size == 64;
     const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
-    tl::SkinnyPlan plan = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
-    const bool skinny_ok = plan.ok;
+    const int impl = skinny_impl();
     const bool tile_ok = tl::tile_supported(M, N, K);
+    // skinny candidates: the decode kernel (M <= 16, any group size), then the
+    // tcgen05 skinny kernel (M <= 32, not 64-wide groups)
+    tl::GemvPlan gp{};
+    if (impl == kImplAuto && M <= tl::kGemvMaxM)
+        gp = tl::plan_gemv(M, N, K, d->sm_count, false, force_sk);
+    tl::SkinnyTcPlan tp{};
+    tl::SkinnyPlan mp{};
+    if (!gp.ok && !g64 && impl != kImplMma) {
+        static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
+        tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
+    }
+    if (!g64 && impl == kImplMma) mp = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
+    const bool skinny_ok = gp.ok || tp.ok || mp.ok;
     int use = path;
     if (use == TL_PATH_AUTO) {
-        use = (M <= skinny_max_m() && skinny_ok && !g64) ? TL_PATH_SKINNY : TL_PATH_TILE;
-        if (use == TL_PATH_TILE && !tile_ok && skinny_ok && !g64) use = TL_PATH_SKINNY;
+        use = (M <= skinny_max_m() && skinny_ok) ? TL_PATH_SKINNY : TL_PATH_TILE;
+        if (use == TL_PATH_TILE && !tile_ok && skinny_ok) use = TL_PATH_SKINNY;
     }
     if (use == TL_PATH_SKINNY) {
-        if (!skinny_ok || g64) return TL_ERR_UNSUPPORTED;
-        if (skinny_impl_tc(M)) {
-            static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
-            tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
-            if (!tp.ok) return TL_ERR_UNSUPPORTED;
+        if (!skinny_ok) return TL_ERR_UNSUPPORTED;
+        if (gp.ok) {
+            tl::GemvArgs a{};
+            a.x = static_cast<const uint16_t *>(x);
+            a.packed = packed;
+            a.scale = static_cast<const uint16_t *>(scale);
+            a.out = out;
+            a.M = (int)M;
+            a.N = (int)N;
+            a.K = (int)K;
+            a.gshift = gshift;
+            a.nh = 0;
+            a.flags = gemv_flags(flags);
+            a.status = d->status;
+            a.wait_limit = wait_limit();
+            return from_cuda(tl::launch_gemv(a, bf, group, out_dtype, gp, st, pdl_enabled()));
+        }
+        if (tp.ok) {
             tl::SkinnyTcArgs a{};
             a.x = static_cast<const uint16_t *>(x);
             a.packed = packed;
@@ -230,7 +263,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
         a.gshift = gshift;
         a.flags = skinny_launch_flags(flags);
         a.status = d->status;
-        return from_cuda(tl::launch_skinny(a, bf, group, out_dtype, plan, st, pdl_enabled()));
+        return from_cuda(tl::launch_skinny(a, bf, group, out_dtype, mp, st, pdl_enabled()));
     }
     if (!tile_ok) return TL_ERR_UNSUPPORTED;
     tl::TileArgs a{};
@@ -268,8 +301,27 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     const bool bf = x_dtype == TL_BF16;
     const bool group = group_size != 0;
     const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
+    static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
+    if (M <= skinny_max_m() && M <= tl::kGemvMaxM && skinny_impl() == kImplAuto) {
+        tl::GemvPlan gp = tl::plan_gemv(M, 2 * N, K, d->sm_count, true, force_sk);
+        if (gp.ok) {
+            tl::GemvArgs a{};
+            a.x = static_cast<const uint16_t *>(x);
+            a.packed = packed;
+            a.scale = static_cast<const uint16_t *>(scale);
+            a.out = out;
+            a.M = (int)M;
+            a.N = (int)(2 * N);
+            a.K = (int)K;
+            a.gshift = gshift;
+            a.nh = (int)N;
+            a.flags = gemv_flags(flags);
+            a.status = d->status;
+            a.wait_limit = wait_limit();
+            return from_cuda(tl::launch_gemv_silu(a, bf, group, out_dtype, gp, st, pdl_enabled()));
+        }
+    }
     if (M <= skinny_max_m() && group_size != 64) {
-        static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, 2 * N, K, d->sm_count, force_sk, per_sm);
         if (tp.ok) {
@@ -306,7 +358,9 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
 tl_status check_packing(const void *t, const void *packed, int64_t N, int64_t K,
                         const int64_t *count) {
     if (N < 0 || K < 0 || K % 4 != 0) return TL_ERR_SHAPE;
+    // N * K must stay representable (and addressable): cap the element count at 2^48
     if (N >= ((int64_t)1 << 40) || K >= ((int64_t)1 << 40)) return TL_ERR_SHAPE;
+    if (K > 0 && N > (((int64_t)1 << 48) / K)) return TL_ERR_SHAPE;
     if (N * K > 0 && (t == nullptr || packed == nullptr)) return TL_ERR_NULL;
     if ((t && !aligned16(t)) || (packed && !aligned16(packed))) return TL_ERR_ALIGN;
     if (count && (reinterpret_cast<uintptr_t>(count) & 7u)) return TL_ERR_ALIGN;
@@ -400,7 +454,7 @@ const char *ternary_status_string(int32_t status) {
     case TL_OK: return "TL_OK";
     case TL_ERR_NULL: return "TL_ERR_NULL: a required pointer is NULL";
     case TL_ERR_SHAPE: return "TL_ERR_SHAPE: invalid or unsupported sizes";
-    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size (0, 64, 128) or path code";
+    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size (0, 64, 128, 256) or path code";
     case TL_ERR_ALIGN: return "TL_ERR_ALIGN: pointer not 16-byte aligned or K % 64 != 0";
     case TL_ERR_VALUE: return "TL_ERR_VALUE: invalid or reserved values present";
     case TL_ERR_CUDA: return "TL_ERR_CUDA: a CUDA call or kernel launch failed";
@@ -415,6 +469,23 @@ int32_t ternary_version(void) { return 100; }
 
 void ternary_test_inject_launch_failures(int32_t n) {
     g_inject_launch_failures.store(n < 0 ? 0 : n);
+}
+
+void ternary_test_set_wait_limit(int64_t cycles, int32_t stall) {
+    g_wait_limit.store(cycles > 0 ? cycles : 0);
+    g_stall.store(stall ? 1 : 0);
+}
+
+tl_status ternary_device_status_async(int32_t *dst, int32_t clear, void *stream) {
+    if (dst == nullptr) return TL_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(dst) & 3u) != 0) return TL_ERR_ALIGN;
+    DevInfo *d = nullptr;
+    tl_status s = current_device(&d, true);
+    if (s != TL_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    s = from_cuda(cudaMemcpyAsync(dst, d->status, sizeof(int), cudaMemcpyDefault, st));
+    if (s == TL_OK && clear) s = from_cuda(cudaMemsetAsync(d->status, 0, sizeof(int), st));
+    return s;
 }
 
 }  // extern "C"

@@ -146,12 +146,16 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
         : "memory");
     return ok != 0;
 }
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Default give-up time of a bounded wait, in SM clock cycles (~0.5 s).
+constexpr long long kWaitLimitDefault = 1ll << 30;
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  long long limit = kWaitLimitDefault) {
     if (mbar_try_wait(bar, parity)) return true;  // fast path: no clock read
     const long long t0 = clock64();
-    for (uint32_t it = 0;; ++it) {
+    for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 200u)) return true;
-        if ((it & 63u) == 63u && clock64() - t0 > (1ll << 30)) return false;
+        if (clock64() - t0 > limit) return false;
     }
 }
 // Copy `bytes` (multiple of 16; both addresses 16-byte aligned) from global

@@ -91,6 +91,45 @@ cudaError_t launch_skinny_tc(const SkinnyTcArgs &a, bool bf, bool group, int out
 cudaError_t launch_skinny_silu(const SkinnyTcArgs &a, bool bf, bool group, int out_dtype,
                                const SkinnyTcPlan &p, cudaStream_t st, bool pdl);
 
+// ------------------------------------------------------------ decode path (gemv.cuh)
+// GemvArgs::flags
+constexpr int kGemvStaticWeights = 1;  // packed / scale may be read before griddepcontrol.wait
+constexpr int kGemvTestStall = 2;      // testing aid: consumers first wait on a barrier nothing arrives on
+
+struct GemvArgs {
+    const uint16_t *x;       // [M,K] fp16 or bf16 bits
+    const uint8_t *packed;   // [N,K/4]
+    const uint16_t *scale;   // fp16 [N] or [N,K/G]
+    void *out;               // [M,N] (gated: [M,nh])
+    int M, N, K;             // N = every stacked row (gated: 2 * nh)
+    int gshift;              // log2 of the group size G (6, 7 or 8) in group mode
+    int nh;                  // gated call: gate rows [0, nh), up rows [nh, 2 nh)
+    int rg;                  // row groups (16 rows) per CTA, from the plan
+    int kc;                  // k per CTA (multiple of 256), from the plan
+    int ws;                  // weight stages in the ring, from the plan
+    int flags;               // kGemv* bits
+    int *status;             // device status word (bounded-wait failures)
+    long long wait_limit;    // give-up time of the main-loop waits, SM cycles
+};
+
+struct GemvPlan {
+    int nt8;    // 8-token MMA tiles (1 or 2)
+    int rg;     // row groups per CTA
+    int tiles;  // row blocks (grid x)
+    int sk;     // K split = cluster size (grid y)
+    int kc;     // k per CTA
+    int ws;     // ring stages
+    bool ok;
+};
+
+constexpr int kGemvMaxM = 16;
+// rows = stacked weight rows (gated: 2 * nh); gated plans pair rows within a CTA
+GemvPlan plan_gemv(int64_t M, int64_t rows, int64_t K, int sm_count, bool gated, int force_sk = 0);
+cudaError_t launch_gemv(const GemvArgs &a, bool bf, bool group, int out_dtype, const GemvPlan &p,
+                        cudaStream_t st, bool pdl);
+cudaError_t launch_gemv_silu(const GemvArgs &a, bool bf, bool group, int out_dtype,
+                             const GemvPlan &p, cudaStream_t st, bool pdl);
+
 // ------------------------------------------------------------ tile path
 struct TileArgs {
     const uint16_t *x;       // [M,K]

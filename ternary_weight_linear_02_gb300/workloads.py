@@ -49,12 +49,40 @@ class Config:
     s_lo: float
     s_hi: float
     p_reserved: float = 0.0
+    layout: str = "plain"   # "plain": one call per projection, each on its own input;
+                            # "fused_mlp": QKV and o as plain calls, gate/up with the
+                            # SiLU-gated product fused, down reading that product
+    rotate: int = 1         # weight sets cycled by the benchmark so a pass exceeds 2x L2
+
+
+@dataclass(frozen=True)
+class Call:
+    """One kernel call of a model layer.  kind: "linear" or "silu_mul";
+    layer: index into Config.layers; src: -1 for an input of its own, else the
+    index of the call (same model layer) whose output it reads."""
+    kind: str
+    layer: int
+    src: int = -1
+
+
+def layer_calls(cfg: "Config") -> tuple:
+    """The calls of one model layer in the config's layout."""
+    if cfg.layout == "fused_mlp":
+        ix = {l.name: i for i, l in enumerate(cfg.layers)}
+        return (Call("linear", ix["qkv"]), Call("linear", ix["o"]),
+                Call("silu_mul", ix["gate_up"]), Call("linear", ix["down"], src=2))
+    return tuple(Call("linear", i) for i in range(len(cfg.layers)))
+
+
+def out_cols(cfg: "Config", c: Call) -> int:
+    n = cfg.layers[c.layer].N
+    return n // 2 if c.kind == "silu_mul" else n
 
 
 CONFIGS = {
     "linear1k": Config(
         "linear1k", "single ternary linear M=1 K=N=1024 fp16 g128",
-        (Layer("linear", 1024, 1024),), 1, (1,), torch.float16, 128, 0.01, 0.05),
+        (Layer("linear", 1024, 1024),), 1, (1,), torch.float16, 128, 0.01, 0.05, rotate=1024),
     "decode7b": Config(
         "decode7b", "7B-shaped decode set (4096/11008), per-channel, bf16",
         (Layer("q", 4096, 4096), Layer("k", 4096, 4096), Layer("v", 4096, 4096),
@@ -66,36 +94,45 @@ CONFIGS = {
         (Layer("q", 1024, 1024), Layer("k", 1024, 1024), Layer("v", 1024, 1024),
          Layer("o", 1024, 1024), Layer("gate", 3072, 1024), Layer("up", 3072, 1024),
          Layer("down", 1024, 3072)),
-        28, (64, 256, 1024), torch.float16, 128, 0.005, 0.05, 0.001),
+        28, (64, 256, 1024), torch.float16, 128, 0.005, 0.05, 0.001, rotate=3),
     "layers27b": Config(
         "layers27b", "27B-class layers (5120/17408), bf16 g128",
         (Layer("attn", 5120, 5120), Layer("up", 17408, 5120),
          Layer("down", 5120, 17408)),
-        1, (1, 8, 32), torch.bfloat16, 128, 0.005, 0.05),
+        1, (1, 8, 32), torch.bfloat16, 128, 0.005, 0.05, rotate=6),
     "stack7b": Config(
         "stack7b", "7B-shaped 28-layer stack, fused QKV and gate/up, per-channel, bf16",
         (Layer("qkv", 4608, 3584, (3584, 512, 512)), Layer("o", 3584, 3584),
          Layer("gate_up", 37888, 3584, (18944, 18944)), Layer("down", 3584, 18944)),
-        28, (1, 16, 64, 256, 2048), torch.bfloat16, 0, 0.005, 0.05),
+        28, (1, 16, 64, 256, 2048), torch.bfloat16, 0, 0.005, 0.05, layout="fused_mlp"),
 }
 
 
 def packed_bytes(cfg: Config) -> int:
     """Packed-weight bytes of one pass over the config's stack (one M)."""
-    return cfg.depth * sum(l.N * l.K // 4 for l in cfg.layers)
+    return cfg.depth * sum(cfg.layers[c.layer].N * cfg.layers[c.layer].K // 4
+                           for c in layer_calls(cfg))
 
 
 def scale_bytes(cfg: Config) -> int:
-    per = (lambda l: 2 * l.N) if cfg.group_size == 0 else (lambda l: 2 * l.N * l.K // cfg.group_size)
-    return cfg.depth * sum(per(l) for l in cfg.layers)
+    def per(l):
+        return 2 * l.N if cfg.group_size == 0 else 2 * l.N * l.K // cfg.group_size
+    return cfg.depth * sum(per(cfg.layers[c.layer]) for c in layer_calls(cfg))
+
+
+def call_bytes(cfg: Config, c: Call, M: int) -> int:
+    """Algorithmic bytes of one call: packed + scales + x + out."""
+    l = cfg.layers[c.layer]
+    sc = 2 * l.N if cfg.group_size == 0 else 2 * l.N * l.K // cfg.group_size
+    return l.N * l.K // 4 + sc + 2 * M * l.K + 2 * M * out_cols(cfg, c)
 
 
 def algorithmic_bytes(cfg: Config, M: int) -> int:
     """Bytes one pass must move at minimum: packed + scales + x + out."""
-    return packed_bytes(cfg) + scale_bytes(cfg) + cfg.depth * sum(
-        2 * M * l.K + 2 * M * l.N for l in cfg.layers)
+    return cfg.depth * sum(call_bytes(cfg, c, M) for c in layer_calls(cfg))
 
 
 def flops(cfg: Config, M: int) -> int:
-    """Effective 2*M*N*K flops of one pass."""
-    return cfg.depth * sum(2 * M * l.N * l.K for l in cfg.layers)
+    """Effective 2*M*N*K flops of one pass (N = every stacked weight row)."""
+    return cfg.depth * sum(2 * M * cfg.layers[c.layer].N * cfg.layers[c.layer].K
+                           for c in layer_calls(cfg))

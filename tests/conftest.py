@@ -30,3 +30,22 @@ def oracle_mod():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean(request):
+    """After every GPU test: no bounded device-side wait gave up during it.  A
+    wait that gives up skips its CTA's stores, so the status word -- not only the
+    tolerance check on stale memory -- must show it."""
+    yield
+    if request.node.get_closest_marker("gpu") is None:
+        return
+    import torch
+    if not torch.cuda.is_available():
+        return
+    import ternary_weight_linear_02_gb300 as tl
+    if tl._lib is None:
+        return
+    torch.cuda.synchronize()
+    code = tl.device_status(clear=True)
+    assert code == 0, f"device status {tl.status_string(code)} after {request.node.nodeid}"

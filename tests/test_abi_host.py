@@ -63,6 +63,8 @@ def test_status_strings(lib):
     for s in range(0, 9):
         assert lib.ternary_status_string(s)
     assert b"unknown" in lib.ternary_status_string(99)
+    # the accepted group sizes are named
+    assert b"(0, 64, 128, 256)" in lib.ternary_status_string(TL_ERR_DTYPE)
     assert lib.ternary_version() >= 100
 
 
@@ -138,6 +140,9 @@ def test_packing_argument_errors(lib):
     assert lib.ternary_unpack(p(B), None, 4, 8, None, None) == TL_ERR_NULL
     assert lib.ternary_pack(p(A + 1), p(B), 4, 8, None, None) == TL_ERR_ALIGN
     assert lib.ternary_unpack(p(B), p(A), 4, 8, p(C + 4), None) == TL_ERR_ALIGN
+    # N * K beyond 2^48 elements: rejected before any product can overflow
+    assert lib.ternary_pack(p(A), p(B), (1 << 39), (1 << 20), None, None) == TL_ERR_SHAPE
+    assert lib.ternary_unpack(p(B), p(A), (1 << 30), (1 << 30), None, None) == TL_ERR_SHAPE
 
 
 def test_injected_launch_failure_reported_before_cuda(lib):

@@ -411,8 +411,10 @@ def test_silu_mul_tile_matches_unfused_calls():
     assert torch.allclose(h, want, rtol=1e-5, atol=1e-6 * float(want.abs().max()))
 
 
-def test_group64_skinny_path_refused():
-    x, p, s = layer_inputs(2, 64, 256, torch.bfloat16, 64, 4)
+def test_group64_skinny_path_refused_above_16_tokens():
+    """64-wide groups run on the decode kernel up to M = 16; the tcgen05 skinny
+    kernel (17..32 tokens) folds scales per 128 k and refuses them."""
+    x, p, s = layer_inputs(20, 64, 256, torch.bfloat16, 64, 4)
     with pytest.raises(tl.TernaryError) as e:
         tl.linear(x, p, s, 64, path="skinny")
     assert e.value.status == 8  # TL_ERR_UNSUPPORTED

@@ -1,8 +1,9 @@
-"""Both decode-shaped kernels against the oracle at every M they can serve.
+"""Every decode-shaped kernel against the oracle at every M it can serve.
 
-The library picks the tcgen05 skinny kernel for M >= 3 and the mma.sync one for
-M <= 2.  TERNARY_SKINNY_IMPL forces one kernel for every M <= 32; it is read once
-per process, so each kernel runs in a child process of its own.
+The library picks the decode kernel of gemv.cuh for M <= 16 and the tcgen05
+skinny kernel for 17 <= M <= 32.  TERNARY_SKINNY_IMPL forces the tcgen05 kernel
+(tc) or the older warp-MMA kernel (mma) for every M <= 32; it is read once per
+process, so each choice runs in a child process of its own.
 """
 import os
 import subprocess
@@ -45,7 +46,7 @@ CHILD = textwrap.dedent("""
 """)
 
 
-@pytest.mark.parametrize("impl", ["tc", "mma"])
+@pytest.mark.parametrize("impl", ["auto", "tc", "mma"])
 def test_skinny_kernel_forced(impl):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
