@@ -206,7 +206,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     // tcgen05 skinny kernel (M <= 32, not 64-wide groups)
     tl::GemvPlan gp{};
     if (impl == kImplAuto && M <= tl::kGemvMaxM)
-        gp = tl::plan_gemv(M, N, K, d->sm_count, false, force_sk);
+        gp = tl::plan_gemv(M, N, K, d->sm_count, false, group, force_sk);
     tl::SkinnyTcPlan tp{};
     tl::SkinnyPlan mp{};
     if (!gp.ok && !g64 && impl != kImplMma) {
@@ -234,9 +234,10 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
             a.gshift = gshift;
             a.nh = 0;
             a.flags = gemv_flags(flags);
+            a.odt = out_dtype;
             a.status = d->status;
             a.wait_limit = wait_limit();
-            return from_cuda(tl::launch_gemv(a, bf, group, out_dtype, gp, st, pdl_enabled()));
+            return from_cuda(tl::launch_gemv(a, bf, group, gp, st, pdl_enabled()));
         }
         if (tp.ok) {
             tl::SkinnyTcArgs a{};
@@ -303,7 +304,7 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
     if (M <= skinny_max_m() && M <= tl::kGemvMaxM && skinny_impl() == kImplAuto) {
-        tl::GemvPlan gp = tl::plan_gemv(M, 2 * N, K, d->sm_count, true, force_sk);
+        tl::GemvPlan gp = tl::plan_gemv(M, 2 * N, K, d->sm_count, true, group_size != 0, force_sk);
         if (gp.ok) {
             tl::GemvArgs a{};
             a.x = static_cast<const uint16_t *>(x);
@@ -316,9 +317,10 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
             a.gshift = gshift;
             a.nh = (int)N;
             a.flags = gemv_flags(flags);
+            a.odt = out_dtype;
             a.status = d->status;
             a.wait_limit = wait_limit();
-            return from_cuda(tl::launch_gemv_silu(a, bf, group, out_dtype, gp, st, pdl_enabled()));
+            return from_cuda(tl::launch_gemv_silu(a, bf, group, gp, st, pdl_enabled()));
         }
     }
     if (M <= skinny_max_m() && group_size != 64) {

@@ -1,6 +1,7 @@
 // gemv.cuh -- the decode-shaped kernel (M <= 16 tokens): fused unpack and
-// accumulate on register-fed warp MMAs, packed weights staged by TMA.  Shared
-// by kern_gemv.cu (plain output) and kern_gemv_silu.cu (SiLU-gated gate/up).
+// accumulate on register-fed warp MMAs, packed weights and x staged by TMA.
+// Shared by kern_gemv.cu (plain output) and kern_gemv_silu.cu (SiLU-gated
+// gate/up).
 //
 // out[m,n] = sum_k t[n,k] x[m,k], scaled per output channel (Qwen2.5-7B
 // ternary-in-vLLM write-up, m.nxbn.cn/news/169761, §3.2, §4.2) or per K group of
@@ -9,22 +10,24 @@
 // t decoded with the code table of the first page's §3.1.
 //
 // Memory-bound design: every packed byte is read from HBM once and decoded
-// once, in registers; the decoded +-1/0 weights are fed straight from
-// registers to mma.sync (m16n8k16, fp32 accumulate), whose cost does not grow
-// with the number of tokens.  Nothing is handed from one warp to another
-// inside the main loop.
+// once, in registers; the decoded +-1/0 weights go straight from registers to
+// mma.sync (m16n8k16, fp32 accumulate), whose cost does not grow with the
+// number of tokens.  Nothing is handed from one warp to another inside the
+// main loop.
 //
-// Work split.  A CTA owns RB = 16*RG weight rows x a K range (a multiple of 256
-// k); the K ranges of a row block are the CTAs of one thread-block cluster
-// (split K <= 8).  The K range is cut into 64-k columns; warp w (of 8) takes
-// the columns at offset 64*(w%4) of every other 256-k stage (stages of parity
-// w/4), and for each of its columns runs every row group of the CTA through
-// that column with the column's x fragments held in registers (loaded straight
-// from global memory one column ahead, so x is never staged or re-read per
-// row).  Warp 8 is the producer: one 2-D TMA per 256-k stage (64 B x RB rows,
-// 64-byte swizzle) into a ring of shared-memory stages; with static weights
-// the ring is filled before griddepcontrol.wait, so under programmatic
-// dependent launch a layer's weights stream while the previous kernel ends.
+// Work split.  A CTA owns RB = 32*RGW weight rows x a K range (a multiple of
+// 256 k); the K ranges of a row block are the CTAs of one thread-block cluster
+// (split K).  Warp 8 is the producer: per 256-k stage one 2-D TMA of the packed
+// weights (64 B x RB rows, 64-byte swizzle) and one 3-D TMA of x (four 64-k
+// chunks x 8*NT8 token rows, 128-byte swizzle; token rows >= M and chunks past
+// K read as zero), into a ring of shared-memory stages.  With static weights
+// the weight half of the first stages is requested before griddepcontrol.wait,
+// so under programmatic dependent launch a layer's weights stream in while the
+// previous kernel ends; x follows after the wait.  Warps 0-7: warp w reads
+// 64-k column w%4 of every stage for the row half w/4 of the CTA (RGW row
+// groups of 16 rows), so a warp keeps only RGW row groups of accumulators --
+// few enough registers for the decode and the MMAs of all its row groups to
+// overlap.
 //
 // Operand mapping for mma.m16n8k16 (A = 16 weight rows, B = x^T, 8 tokens per
 // n-tile).  Lane (g = lane/4, c = lane%4) reads the 32-bit word c (16 codes) of
@@ -39,11 +42,11 @@
 // group -> each column's MMAs start from zero and are folded into the row's
 // fp32 total with that group's scale.
 //
-// Reduction: the 8 warps' partial tiles are summed in warp order through the
-// (then idle) ring; split K across the cluster pushes each CTA's partial rows
-// into the owning CTA's shared memory (st.shared::cluster) and the owner sums
-// them in rank order.  The same inputs give bit-identical outputs, and
-// nothing is allocated.
+// Reduction: the four column warps of a row half are summed in column order
+// through the (then idle) ring; split K across the cluster pushes each CTA's
+// partial rows into the owning CTA's shared memory (st.shared::cluster) and the
+// owner sums them in rank order.  The same inputs give bit-identical outputs,
+// and nothing is allocated.
 //
 // Every mbarrier wait is bounded (give-up time from the launch arguments).  A
 // wait that gives up sets the device status word; the CTA stops, the producer
@@ -59,26 +62,37 @@
 namespace tl {
 namespace gemv {
 
-constexpr int kWarps = 8;                   // consumer warps
+constexpr int kWarps = 8;                   // consumer warps: 4 columns x 2 row halves
 constexpr int kThreads = 32 * (kWarps + 1); // + the producer warp
-constexpr int kStageK = 256;                // k per weight stage: a 64-byte box per row
+constexpr int kStageK = 256;                // k per stage: a 64-byte weight box per row
 constexpr int kRingBytes = 96 * 1024;
-constexpr int kMaxStages = 24;
+constexpr int kMaxStages = 16;
+
+// Row groups (16 rows) per warp the kernel is compiled for: 1..4 (RB = 32..128
+// rows per CTA).  Four row groups of accumulators and code words per warp keep
+// the decode and the MMAs of a column overlapping (measured: more row groups per
+// warp serialise them).
+constexpr int kRgwMax = 4;
 
 template <int NT8>
 struct Cfg {
-    static constexpr int RGMAX = NT8 == 1 ? 8 : 4;  // row groups per CTA (16 rows each)
-    static constexpr int MP = 8 * NT8;              // padded tokens
-    static constexpr int RBMAX = 16 * RGMAX;
-    // split-K receive rows: sk * ceil(RB / sk) <= RB + 8 (or gated: 2 * sk * ceil(RB/2 / sk))
+    static constexpr int MP = 8 * NT8;               // padded tokens
+    static constexpr int RBMAX = 32 * kRgwMax;       // rows per CTA at most
+    static constexpr int XSTAGE = 4 * MP * 128;      // x bytes per stage: 4 chunks x MP rows x 128 B
+    // split-K receive rows: sk * ceil(RB / sk) <= RB + 8 (gated: 2 * sk * ceil(RB/2 / sk))
     static constexpr int RECV_FLOATS = (RBMAX + 16) * MP;
     static constexpr int RECV_OFF = kRingBytes;
-    static constexpr int FLAG_OFF = RECV_OFF + RECV_FLOATS * 4;       // 8 abort flags (one per rank)
+    static constexpr int FLAG_OFF = RECV_OFF + RECV_FLOATS * 4;  // 8 abort flags (one per rank)
     static constexpr int BAR_OFF = FLAG_OFF + 64;
     static constexpr int SMEM = BAR_OFF + (2 * kMaxStages + 2) * 8 + 16 + 1024;
-    static_assert(kWarps * RBMAX * MP * 4 <= kRingBytes, "reduction tiles fit in the ring");
+    static_assert(kWarps * (RBMAX / 2) * MP * 4 <= kRingBytes, "reduction tiles fit in the ring");
     static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
 };
+
+// bytes of one ring stage (x part first, 1024-aligned; then the weight part)
+__host__ __device__ constexpr int stage_stride(int nt8, int rgw) {
+    return 4 * 8 * nt8 * 128 + 64 * 32 * rgw;
+}
 
 // ------------------------------------------------------------------ device helpers
 template <bool BF>
@@ -133,6 +147,9 @@ __device__ __forceinline__ void cl_st_u32(uint32_t addr, uint32_t v) {
 __device__ __forceinline__ void cl_arrive_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cl_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cl_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
@@ -141,6 +158,17 @@ __device__ __forceinline__ void cl_wait_acquire() {
 }
 
 __device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
+
+// fp32 -> out element: fp16 / bf16 (round to nearest even) or fp32
+__device__ __forceinline__ void store_out(int odt, void *base, int64_t idx, float v) {
+    if (odt == 0) OutStore<0>::st(base, idx, v);
+    else if (odt == 1) OutStore<1>::st(base, idx, v);
+    else OutStore<2>::st(base, idx, v);
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t *p) {
+    return *reinterpret_cast<const uint4 *>(p);
+}
 
 // x[n, k .. k+16) of token n as the four (b0, b1) pairs of MMA i = 0..3:
 // b0 = (x[k+i], x[k+i+8]), b1 = (x[k+i+4], x[k+i+12])
@@ -156,11 +184,16 @@ __device__ __forceinline__ void x_frag(const uint4 &lo, const uint4 &hi, uint32_
     b[3][1] = __byte_perm(lo.w, hi.w, 0x7632);  // x7, x15
 }
 
-template <int NT8, bool BF, bool GROUP, int OUT, bool SILU>
+template <int NT8, int RGW, bool BF, bool GROUP, bool SILU>
 __global__ void __launch_bounds__(kThreads, 2)
-    gemv_kernel(const __grid_constant__ CUtensorMap tmw, GemvArgs a) {
+    gemv_kernel(const __grid_constant__ CUtensorMap tmw, const __grid_constant__ CUtensorMap tmx,
+                GemvArgs a) {
     using C = Cfg<NT8>;
-    constexpr int RGMAX = C::RGMAX, MP = C::MP;
+    constexpr int MP = C::MP;
+    constexpr int RB = 32 * RGW, PH = RB / 2;   // rows per CTA; rows per half
+    constexpr int XST = C::XSTAGE, WST = 64 * RB, STRIDE = XST + WST;
+    static_assert(STRIDE == stage_stride(NT8, RGW), "stage layout");
+    static_assert(RGW >= 1 && RGW <= kRgwMax, "row groups per warp");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -174,11 +207,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int RG = a.rg, RB = 16 * RG, PH = RB / 2;
     const int rank = blockIdx.y, sk = gridDim.y;
     const int k0 = rank * a.kc, k1 = min(a.K, k0 + a.kc);
     const int nst = (k1 - k0 + kStageK - 1) / kStageK;
-    const int stage_bytes = 64 * RB;
     // plain: rows [n0, n0 + RB); gated: gate rows [j0, j0 + PH) then up rows [nh + j0, ...)
     const int n0 = blockIdx.x * RB, j0 = blockIdx.x * PH;
     const long long lim = a.wait_limit;
@@ -187,13 +218,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.ws; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 4);  // the four warps that read a stage
+            mbar_init(&empty[i], kWarps);
         }
         mbar_init(never, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kWarps && lane == 0) tc::prefetch_tmap(&tmw);
+    if (warp == kWarps && lane == 0) {
+        tc::prefetch_tmap(&tmw);
+        tc::prefetch_tmap(&tmx);
+    }
     __syncthreads();
     pdl_launch_dependents();
 
@@ -202,41 +236,58 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (a.status) atomicExch(a.status, kStatusTimeout);
     };
 
-    float acc[RGMAX][NT8][4];
-#pragma unroll
-    for (int r = 0; r < RGMAX; ++r)
-#pragma unroll
-        for (int t = 0; t < NT8; ++t)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[r][t][e] = 0.f;
-
-    // weight row (global) of CTA row r, and whether it exists
+    // weight row (global) of CTA row r
     auto wrow = [&](int r) -> int {
         if constexpr (SILU) return r < PH ? j0 + r : a.nh + j0 + (r - PH);
         else return n0 + r;
     };
 
+    float acc[RGW][NT8][4];
+#pragma unroll
+    for (int r = 0; r < RGW; ++r)
+#pragma unroll
+        for (int t = 0; t < NT8; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[r][t][e] = 0.f;
+
     if (warp == kWarps) {
-        // ------------------------------------------------ producer: TMA of weight stages
+        // ------------------------------------------------ producer: TMA of weight and x stages
         if (lane == 0) {
-            if (!(a.flags & kGemvStaticWeights)) pdl_wait();
-            int issued = 0;
+            const bool static_w = (a.flags & kGemvStaticWeights) != 0;
+            if (!static_w) pdl_wait();
+            auto issue_w = [&](int s) {
+                uint8_t *dst = ring + (size_t)(s % a.ws) * STRIDE + XST;
+                const int kb = (k0 >> 2) + s * 64;  // byte column of the stage
+                if constexpr (SILU) {
+                    tc::tma_load_2d(dst, &tmw, kb, j0, &full[s % a.ws]);
+                    tc::tma_load_2d(dst + WST / 2, &tmw, kb, a.nh + j0, &full[s % a.ws]);
+                } else {
+                    tc::tma_load_2d(dst, &tmw, kb, n0, &full[s % a.ws]);
+                }
+            };
+            auto issue_x = [&](int s) {
+                uint8_t *dst = ring + (size_t)(s % a.ws) * STRIDE;
+                tc::tma_load_3d(dst, &tmx, 0, 0, (k0 >> 6) + s * 4, &full[s % a.ws]);
+            };
+            // the first stages: weights now (static weights: before the wait), x after it
+            const int pre = nst < a.ws ? nst : a.ws;
+            for (int s = 0; s < pre; ++s) {
+                mbar_arrive_expect_tx(&full[s], (uint32_t)STRIDE);
+                issue_w(s);
+            }
+            if (static_w) pdl_wait();  // x belongs to the previous kernel until here
+            for (int s = 0; s < pre; ++s) issue_x(s);
+            int issued = pre;
             bool ok = true;
-            for (int s = 0; s < nst; ++s) {
+            for (int s = pre; s < nst; ++s) {
                 const int slot = s % a.ws;
-                if (s >= a.ws && (*abort_flag || !mbar_wait_bounded(&empty[slot], ((s / a.ws) - 1) & 1, lim))) {
+                if (*abort_flag || !mbar_wait_bounded(&empty[slot], ((s / a.ws) - 1) & 1, lim)) {
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)stage_bytes);
-                uint8_t *dst = ring + (size_t)slot * stage_bytes;
-                const int kb = (k0 >> 2) + s * 64;  // byte column of the stage
-                if constexpr (SILU) {
-                    tc::tma_load_2d(dst, &tmw, kb, j0, &full[slot]);
-                    tc::tma_load_2d(dst + stage_bytes / 2, &tmw, kb, a.nh + j0, &full[slot]);
-                } else {
-                    tc::tma_load_2d(dst, &tmw, kb, n0, &full[slot]);
-                }
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)STRIDE);
+                issue_w(s);
+                issue_x(s);
                 ++issued;
             }
             if (!ok) give_up();
@@ -246,61 +297,51 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
     } else {
         // ------------------------------------------------ consumers
-        pdl_wait();  // x (and out) belong to the previous kernel until here
-        const int par = warp >> 2, cw = warp & 3;
-        uint4 xr[NT8][2];
-        uint32_t scn[RGMAX];  // next column's group scales: row g (low half), row g + 8 (high half)
-        auto load_x = [&](int kcol) {
-#pragma unroll
-            for (int t = 0; t < NT8; ++t) {
-                const int n = t * 8 + g;
-                if (n < a.M && kcol < k1) {
-                    const uint16_t *p = a.x + (int64_t)n * a.K + kcol + 16 * c;
-                    xr[t][0] = ldg_nc_v4(p);
-                    xr[t][1] = ldg_nc_v4(p + 8);
-                } else {
-                    xr[t][0] = make_uint4(0, 0, 0, 0);
-                    xr[t][1] = xr[t][0];
-                }
-            }
-        };
+        const int cw = warp & 3;     // 64-k column of every stage
+        const int half = warp >> 2;  // rows [half * PH, half * PH + PH) of the CTA
+        // this lane's offsets inside a stage: x (128-byte swizzle: 16-byte unit u of
+        // token row n at u ^ (n & 7), and n & 7 == g) and weights (64-byte swizzle:
+        // 16-byte chunk j of row q at j ^ ((q >> 1) & 3), and for every row this lane
+        // reads, (q >> 1) & 3 == (g >> 1) & 3)
+        const int xo_lo = (cw * MP + g) * 128 + (((2 * c) ^ g) << 4);
+        const int xo_hi = (cw * MP + g) * 128 + (((2 * c + 1) ^ g) << 4);
+        const int wo = XST + (half * PH + g) * 64 + ((cw ^ ((g >> 1) & 3)) << 4) + 4 * c;
+        uint32_t scn[RGW];  // next column's group scales: row g (low half), row g + 8 (high half)
         auto load_sc = [&](int kcol) {
             if constexpr (GROUP) {
                 const int ngk = a.K >> a.gshift, gi = kcol >> a.gshift;
 #pragma unroll
-                for (int r = 0; r < RGMAX; ++r) {
+                for (int r = 0; r < RGW; ++r) {
                     uint32_t v = 0;
-                    if (r < RG && kcol < k1) {
-                        const int lo = wrow(r * 16 + g), hi = wrow(r * 16 + g + 8);
-                        const uint32_t slo = lo < a.N ? (uint32_t)a.scale[(int64_t)lo * ngk + gi] : 0u;
-                        const uint32_t shi = hi < a.N ? (uint32_t)a.scale[(int64_t)hi * ngk + gi] : 0u;
+                    if (kcol < k1) {
+                        const int rlo = wrow(half * PH + r * 16 + g);
+                        const int rhi = wrow(half * PH + r * 16 + g + 8);
+                        const uint32_t slo = rlo < a.N ? (uint32_t)a.scale[(int64_t)rlo * ngk + gi] : 0u;
+                        const uint32_t shi = rhi < a.N ? (uint32_t)a.scale[(int64_t)rhi * ngk + gi] : 0u;
                         v = slo | (shi << 16);
                     }
                     scn[r] = v;
                 }
             }
         };
-        int kcol = k0 + par * kStageK + cw * 64;
-        load_x(kcol);
-        load_sc(kcol);
+        load_sc(k0 + cw * 64);
         bool ok = true;
         if (a.flags & kGemvTestStall) {
             // testing aid: a wait on a barrier nothing arrives on runs out
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(never, 0, lim));
             if (!ok && lane == 0) give_up();
         }
-        for (int s = par; ok && s < nst; s += 2) {
+        for (int s = 0; ok && s < nst; ++s) {
             const int slot = s % a.ws;
-            const int kc_now = kcol;
-            uint32_t b[NT8][4][2];
+            const int kcol = k0 + s * kStageK + cw * 64;
+            uint32_t sc[RGW];
 #pragma unroll
-            for (int t = 0; t < NT8; ++t) x_frag(xr[t][0], xr[t][1], b[t]);
-            uint32_t sc[RGMAX];
+            for (int r = 0; r < RGW; ++r) sc[r] = 0u;
+            if constexpr (GROUP) {
 #pragma unroll
-            for (int r = 0; r < RGMAX; ++r) sc[r] = GROUP ? scn[r] : 0u;
-            kcol += 2 * kStageK;
-            load_x(kcol);  // next column of this warp, in flight during this one
-            load_sc(kcol);
+                for (int r = 0; r < RGW; ++r) sc[r] = scn[r];
+                load_sc(kcol + kStageK);  // next stage's column, in flight during this one
+            }
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (s / a.ws) & 1, lim))) {
                 if (lane == 0) give_up();
                 ok = false;
@@ -310,24 +351,34 @@ __global__ void __launch_bounds__(kThreads, 2)
                 ok = false;
                 break;
             }
-            if (kc_now < k1) {
-                const uint8_t *st = ring + (size_t)slot * stage_bytes;
+            if (kcol < k1) {
+                const uint8_t *st = ring + (size_t)slot * STRIDE;
+                uint32_t b[NT8][4][2];
 #pragma unroll
-                for (int r = 0; r < RGMAX; ++r) {
-                    if (r >= RG) break;
-                    const int rlo = r * 16 + g, rhi = rlo + 8;
-                    // 64-byte swizzle: 16-byte chunk j of row q sits at chunk j ^ ((q >> 1) & 3)
-                    const uint32_t wlo = *reinterpret_cast<const uint32_t *>(
-                        st + rlo * 64 + ((cw ^ ((rlo >> 1) & 3)) << 4) + 4 * c);
-                    const uint32_t whi = *reinterpret_cast<const uint32_t *>(
-                        st + rhi * 64 + ((cw ^ ((rhi >> 1) & 3)) << 4) + 4 * c);
-                    const uint32_t zlo = sign_nz(wlo), zhi = sign_nz(whi);
-                    if constexpr (GROUP) {
+                for (int t = 0; t < NT8; ++t) {
+                    const uint4 lo = lds128(st + xo_lo + t * 8 * 128);
+                    const uint4 hi = lds128(st + xo_hi + t * 8 * 128);
+                    x_frag(lo, hi, b[t]);
+                }
+                uint32_t zlo[RGW], zhi[RGW];
+#pragma unroll
+                for (int r = 0; r < RGW; ++r) {
+                    zlo[r] = *reinterpret_cast<const uint32_t *>(st + wo + r * 1024);
+                    zhi[r] = *reinterpret_cast<const uint32_t *>(st + wo + r * 1024 + 512);
+                }
+#pragma unroll
+                for (int r = 0; r < RGW; ++r) {
+                    zlo[r] = sign_nz(zlo[r]);
+                    zhi[r] = sign_nz(zhi[r]);
+                }
+                if constexpr (GROUP) {
+#pragma unroll
+                    for (int r = 0; r < RGW; ++r) {
                         float d[NT8][4];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const uint32_t a0 = pair2(zlo, i), a1 = pair2(zhi, i);
-                            const uint32_t a2 = pair2(zlo, i + 4), a3 = pair2(zhi, i + 4);
+                            const uint32_t a0 = pair2(zlo[r], i), a1 = pair2(zhi[r], i);
+                            const uint32_t a2 = pair2(zlo[r], i + 4), a3 = pair2(zhi[r], i + 4);
 #pragma unroll
                             for (int t = 0; t < NT8; ++t) {
                                 if (i == 0)
@@ -345,11 +396,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                             acc[r][t][2] = fmaf(shi, d[t][2], acc[r][t][2]);
                             acc[r][t][3] = fmaf(shi, d[t][3], acc[r][t][3]);
                         }
-                    } else {
+                    }
+                } else {
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const uint32_t a0 = pair2(zlo, i), a1 = pair2(zhi, i);
-                            const uint32_t a2 = pair2(zlo, i + 4), a3 = pair2(zhi, i + 4);
+                    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+                        for (int r = 0; r < RGW; ++r) {
+                            const uint32_t a0 = pair2(zlo[r], i), a1 = pair2(zhi[r], i);
+                            const uint32_t a2 = pair2(zlo[r], i + 4), a3 = pair2(zhi[r], i + 4);
 #pragma unroll
                             for (int t = 0; t < NT8; ++t)
                                 mma16816<BF>(acc[r][t], a0, a1, a2, a3, b[t][i][0], b[t][i][1]);
@@ -364,33 +418,34 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ------------------------------------------------ reduction and epilogue
     __syncthreads();  // every stage consumed (or abandoned) and no copy in flight
-    pdl_wait();       // (the producer warp stores below too)
+    pdl_wait();       // out belongs to the previous kernel until here
     const bool aborted = *abort_flag != 0;
-    float *red = reinterpret_cast<float *>(ring);  // [warp][RB][MP]
+    float *red = reinterpret_cast<float *>(ring);  // [warp][PH][MP]: a warp's rows of its half
     if (warp < kWarps && !aborted) {
 #pragma unroll
-        for (int r = 0; r < RGMAX; ++r) {
-            if (r >= RG) break;
-            const int rlo = r * 16 + g;
+        for (int r = 0; r < RGW; ++r) {
+            const int rl = r * 16 + g;
 #pragma unroll
             for (int t = 0; t < NT8; ++t) {
-                float *p = red + ((size_t)warp * RB + rlo) * MP + t * 8 + 2 * c;
+                float *p = red + ((size_t)warp * PH + rl) * MP + t * 8 + 2 * c;
                 *reinterpret_cast<float2 *>(p) = make_float2(acc[r][t][0], acc[r][t][1]);
                 *reinterpret_cast<float2 *>(p + 8 * MP) = make_float2(acc[r][t][2], acc[r][t][3]);
             }
         }
     }
     __syncthreads();
-    // the CTA's partial of row r, token m: the 8 warps summed in warp order
+    // the CTA's partial of row r, token m: its half's four column warps summed in order
     auto part = [&](int r, int m) {
+        const int h = r >= PH ? 1 : 0, rl = r - h * PH;
         float v = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += red[((size_t)w * RB + r) * MP + m];
+        for (int q = 0; q < 4; ++q) v += red[((size_t)(h * 4 + q) * PH + rl) * MP + m];
         return v;
     };
     // final value (scaled) of stacked row r from its summed partial
     auto scaled = [&](int r, float v) {
         if constexpr (GROUP) {
+            (void)r;
             return 0.5f * v;  // group scales are folded in; the operand was 2t
         } else {
             const int n = wrow(r);
@@ -406,14 +461,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                     const int j = j0 + p;
                     if (j >= a.nh) continue;
                     const float gv = scaled(p, part(p, m)), uv = scaled(PH + p, part(PH + p, m));
-                    OutStore<OUT>::st(a.out, (int64_t)m * a.nh + j, silu(gv) * uv);
+                    store_out(a.odt, a.out, (int64_t)m * a.nh + j, silu(gv) * uv);
                 }
             } else {
                 for (int idx = threadIdx.x; idx < RB * a.M; idx += kThreads) {
                     const int m = idx / RB, r = idx - m * RB;
                     const int n = n0 + r;
                     if (n >= a.N) continue;
-                    OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, scaled(r, part(r, m)));
+                    store_out(a.odt, a.out, (int64_t)m * a.N + n, scaled(r, part(r, m)));
                 }
             }
         }
@@ -422,8 +477,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ------------------------------------------------ split K over the cluster
     // owner q holds rows [q*RB/sk, (q+1)*RB/sk) (gated: pairs [q*PH/sk, (q+1)*PH/sk))
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // phase 1: every peer runs
-    const int span = SILU ? PH : RB;
+    cl_wait();  // phase 1: every peer runs
+    constexpr int span = SILU ? PH : RB;
     const int SL = (span + sk - 1) / sk;
     auto owner = [&](int p) {
         int q = (p * sk) / span;
@@ -432,17 +487,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         return q;
     };
     if (!aborted) {
-        if constexpr (SILU) {
-            for (int idx = threadIdx.x; idx < RB * a.M; idx += kThreads) {
-                const int m = idx / RB, r = idx - m * RB;
-                const int half = r >= PH ? 1 : 0, p = r - half * PH;
+        for (int idx = threadIdx.x; idx < RB * a.M; idx += kThreads) {
+            const int m = idx / RB, r = idx - m * RB;
+            if constexpr (SILU) {
+                const int hf = r >= PH ? 1 : 0, p = r - hf * PH;
                 const int q = owner(p), pp = p - (q * span) / sk;
-                const float *slot = recv + ((size_t)(rank * 2 + half) * SL + pp) * MP + m;
+                const float *slot = recv + ((size_t)(rank * 2 + hf) * SL + pp) * MP + m;
                 cl_st_f32(cl_map(smem_u32(slot), (uint32_t)q), part(r, m));
-            }
-        } else {
-            for (int idx = threadIdx.x; idx < RB * a.M; idx += kThreads) {
-                const int m = idx / RB, r = idx - m * RB;
+            } else {
                 const int q = owner(r), rr = r - (q * span) / sk;
                 const float *slot = recv + ((size_t)rank * SL + rr) * MP + m;
                 cl_st_f32(cl_map(smem_u32(slot), (uint32_t)q), part(r, m));
@@ -467,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 gv += recv[((size_t)(q * 2) * SL + pp) * MP + m];
                 uv += recv[((size_t)(q * 2 + 1) * SL + pp) * MP + m];
             }
-            OutStore<OUT>::st(a.out, (int64_t)m * a.nh + j, silu(scaled(p, gv)) * scaled(PH + p, uv));
+            store_out(a.odt, a.out, (int64_t)m * a.nh + j, silu(scaled(p, gv)) * scaled(PH + p, uv));
         }
     } else {
         for (int idx = threadIdx.x; idx < plen * a.M; idx += kThreads) {
@@ -476,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (n >= a.N) continue;
             float v = 0.f;
             for (int q = 0; q < sk; ++q) v += recv[((size_t)q * SL + rr) * MP + m];
-            OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, scaled(r, v));
+            store_out(a.odt, a.out, (int64_t)m * a.N + n, scaled(r, v));
         }
     }
 }
@@ -502,24 +554,36 @@ inline EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int NT8, bool BF, bool GROUP, int OUT, bool SILU>
+template <int NT8, int RGW, bool BF, bool GROUP, bool SILU>
 cudaError_t launch_one(const GemvArgs &a, const GemvPlan &p, cudaStream_t st, bool pdl) {
     using C = Cfg<NT8>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
-    const int RB = 16 * p.rg;
+    constexpr int RB = 32 * RGW;
     // packed [N, K/4] bytes; box = 64 bytes (256 k) x RB rows (gated: RB/2 rows, loaded
     // twice per stage: gate rows and up rows); rows >= N and bytes >= K/4 read as zero
     CUtensorMap mw;
-    const cuuint64_t dims[2] = {(cuuint64_t)(a.K / 4), (cuuint64_t)a.N};
-    const cuuint64_t strides[1] = {(cuuint64_t)(a.K / 4)};
-    const cuuint32_t box[2] = {64u, (cuuint32_t)(SILU ? RB / 2 : RB)};
-    const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+    const cuuint64_t wdims[2] = {(cuuint64_t)(a.K / 4), (cuuint64_t)a.N};
+    const cuuint64_t wstrides[1] = {(cuuint64_t)(a.K / 4)};
+    const cuuint32_t wbox[2] = {64u, (cuuint32_t)(SILU ? RB / 2 : RB)};
+    const cuuint32_t estr2[2] = {1, 1};
+    CUresult r = enc(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(a.packed), wdims,
+                     wstrides, wbox, estr2, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = gemv_kernel<NT8, BF, GROUP, OUT, SILU>;
+    // x [M, K] 16-bit viewed as [K/64 chunks][M rows][64 k]: one box = 4 chunks x MP
+    // token rows x 64 k (rows >= M and chunks past K read as zero)
+    CUtensorMap mx;
+    const cuuint64_t xdims[3] = {64u, (cuuint64_t)a.M, (cuuint64_t)(a.K / 64)};
+    const cuuint64_t xstrides[2] = {(cuuint64_t)a.K * 2, 128u};
+    const cuuint32_t xbox[3] = {64u, (cuuint32_t)C::MP, 4u};
+    const cuuint32_t estr3[3] = {1, 1, 1};
+    r = enc(&mx, BF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+            const_cast<uint16_t *>(a.x), xdims, xstrides, xbox, estr3, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    auto kern = gemv_kernel<NT8, RGW, BF, GROUP, SILU>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     GemvArgs b = a;
@@ -547,27 +611,30 @@ cudaError_t launch_one(const GemvArgs &a, const GemvPlan &p, cudaStream_t st, bo
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, kern, mw, b);
+    return cudaLaunchKernelEx(&cfg, kern, mw, mx, b);
 }
 
+// one instantiation per row-group count per warp (GemvPlan::rg = 2 * RGW row groups per CTA)
 template <int NT8, bool BF, bool GROUP, bool SILU>
-cudaError_t launch_out(const GemvArgs &a, int out_dtype, const GemvPlan &p, cudaStream_t st,
-                       bool pdl) {
-    switch (out_dtype) {
-    case 0: return launch_one<NT8, BF, GROUP, 0, SILU>(a, p, st, pdl);
-    case 1: return launch_one<NT8, BF, GROUP, 1, SILU>(a, p, st, pdl);
-    default: return launch_one<NT8, BF, GROUP, 2, SILU>(a, p, st, pdl);
+cudaError_t launch_rgw(const GemvArgs &a, const GemvPlan &p, cudaStream_t st, bool pdl) {
+    switch (p.rg / 2) {
+    case 1: return launch_one<NT8, 1, BF, GROUP, SILU>(a, p, st, pdl);
+    case 2: return launch_one<NT8, 2, BF, GROUP, SILU>(a, p, st, pdl);
+    case 3: return launch_one<NT8, 3, BF, GROUP, SILU>(a, p, st, pdl);
+    case 4: return launch_one<NT8, 4, BF, GROUP, SILU>(a, p, st, pdl);
+    default: return cudaErrorInvalidValue;
     }
 }
 
 template <bool BF, bool SILU>
-cudaError_t launch_dtype(const GemvArgs &a, bool group, int out_dtype, const GemvPlan &p,
-                         cudaStream_t st, bool pdl) {
+cudaError_t launch_dtype(const GemvArgs &a, bool group, const GemvPlan &p, cudaStream_t st,
+                         bool pdl) {
+    if (p.rg % 2 != 0) return cudaErrorInvalidValue;
     if (p.nt8 == 1)
-        return group ? launch_out<1, BF, true, SILU>(a, out_dtype, p, st, pdl)
-                     : launch_out<1, BF, false, SILU>(a, out_dtype, p, st, pdl);
-    return group ? launch_out<2, BF, true, SILU>(a, out_dtype, p, st, pdl)
-                 : launch_out<2, BF, false, SILU>(a, out_dtype, p, st, pdl);
+        return group ? launch_rgw<1, BF, true, SILU>(a, p, st, pdl)
+                     : launch_rgw<1, BF, false, SILU>(a, p, st, pdl);
+    return group ? launch_rgw<2, BF, true, SILU>(a, p, st, pdl)
+                 : launch_rgw<2, BF, false, SILU>(a, p, st, pdl);
 }
 
 }  // namespace gemv

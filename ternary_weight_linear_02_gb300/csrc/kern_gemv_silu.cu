@@ -8,10 +8,10 @@
 
 namespace tl {
 
-cudaError_t launch_gemv_silu(const GemvArgs &a, bool bf, bool group, int out_dtype,
-                             const GemvPlan &p, cudaStream_t st, bool pdl) {
-    return bf ? gemv::launch_dtype<true, true>(a, group, out_dtype, p, st, pdl)
-              : gemv::launch_dtype<false, true>(a, group, out_dtype, p, st, pdl);
+cudaError_t launch_gemv_silu(const GemvArgs &a, bool bf, bool group, const GemvPlan &p,
+                             cudaStream_t st, bool pdl) {
+    return bf ? gemv::launch_dtype<true, true>(a, group, p, st, pdl)
+              : gemv::launch_dtype<false, true>(a, group, p, st, pdl);
 }
 
 }  // namespace tl

@@ -108,6 +108,7 @@ struct GemvArgs {
     int kc;                  // k per CTA (multiple of 256), from the plan
     int ws;                  // weight stages in the ring, from the plan
     int flags;               // kGemv* bits
+    int odt;                 // output dtype: 0 fp16, 1 bf16, 2 fp32
     int *status;             // device status word (bounded-wait failures)
     long long wait_limit;    // give-up time of the main-loop waits, SM cycles
 };
@@ -124,11 +125,13 @@ struct GemvPlan {
 
 constexpr int kGemvMaxM = 16;
 // rows = stacked weight rows (gated: 2 * nh); gated plans pair rows within a CTA
-GemvPlan plan_gemv(int64_t M, int64_t rows, int64_t K, int sm_count, bool gated, int force_sk = 0);
-cudaError_t launch_gemv(const GemvArgs &a, bool bf, bool group, int out_dtype, const GemvPlan &p,
-                        cudaStream_t st, bool pdl);
-cudaError_t launch_gemv_silu(const GemvArgs &a, bool bf, bool group, int out_dtype,
-                             const GemvPlan &p, cudaStream_t st, bool pdl);
+GemvPlan plan_gemv(int64_t M, int64_t rows, int64_t K, int sm_count, bool gated, bool group,
+                   int force_sk = 0);
+// a.odt selects the output dtype
+cudaError_t launch_gemv(const GemvArgs &a, bool bf, bool group, const GemvPlan &p, cudaStream_t st,
+                        bool pdl);
+cudaError_t launch_gemv_silu(const GemvArgs &a, bool bf, bool group, const GemvPlan &p,
+                             cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------ tile path
 struct TileArgs {

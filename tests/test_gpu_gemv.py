@@ -45,10 +45,10 @@ CASES = [
     (1, 200, 192, BF16, 64, F32),      # three columns: some warps idle
     (1, 4096, 4096, BF16, 0, F32),     # q/o-shaped
     (1, 300, 18944, BF16, 0, F32),     # long K, split K over the cluster
-    (1, 129, 1088, F16, 128, F32),     # 4.25 stages: the last stage holds one column
+    (1, 129, 1088, F16, 64, F32),      # 4.25 stages: the last stage holds one column
     (2, 64, 8192, BF16, 256, F32),     # one row block, split K 8
     (2, 1000, 2048, F16, 0, F16),
-    (3, 33, 320, BF16, 128, BF16),
+    (3, 33, 384, BF16, 128, BF16),
     (4, 11008, 4096, BF16, 0, F32),    # gate/up-shaped
     (4, 513, 1024, F16, 256, F32),
     (5, 300, 3584, BF16, 128, F32),
