@@ -71,8 +71,14 @@ constexpr int kMaxStages = 16;
 // Row groups (16 rows) per warp the kernel is compiled for: 1..4 (RB = 32..128
 // rows per CTA).  Four row groups of accumulators and code words per warp keep
 // the decode and the MMAs of a column overlapping (measured: more row groups per
-// warp serialise them).
+// warp serialise them).  The software pipeline holds two stages' code words and
+// x in registers; the largest counts that compile without spilling at two CTAs
+// per SM (96 registers) are below -- group scales also hold each column's
+// partials and the next column's scales.
 constexpr int kRgwMax = 4;
+__host__ __device__ constexpr int rgw_max(int nt8, bool group) {
+    return nt8 == 1 ? (group ? 2 : 4) : (group ? 1 : 3);
+}
 
 template <int NT8>
 struct Cfg {
@@ -331,8 +337,36 @@ __global__ void __launch_bounds__(kThreads, 2)
             ok = __all_sync(0xffffffffu, mbar_wait_bounded(never, 0, lim));
             if (!ok && lane == 0) give_up();
         }
-        for (int s = 0; ok && s < nst; ++s) {
+        // Software pipeline over stages: the next stage is waited for and moved into
+        // registers (its code words and x) before this stage's decode and MMAs, and its
+        // ring slot is handed back as soon as the loads are done, so shared-memory
+        // latency and the barrier wait overlap the arithmetic.
+        uint32_t wc[2 * RGW], wn[2 * RGW];  // code words (lo, hi per row group): current, next
+        uint4 xc[NT8][2], xn[NT8][2];       // x (two 16-byte halves per token tile)
+        auto fetch = [&](int s, uint32_t (&w)[2 * RGW], uint4 (&x)[NT8][2]) -> bool {
             const int slot = s % a.ws;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (s / a.ws) & 1, lim))) {
+                if (lane == 0) give_up();
+                return false;
+            }
+            const uint8_t *st = ring + (size_t)slot * STRIDE;
+#pragma unroll
+            for (int t = 0; t < NT8; ++t) {
+                x[t][0] = lds128(st + xo_lo + t * 8 * 128);
+                x[t][1] = lds128(st + xo_hi + t * 8 * 128);
+            }
+#pragma unroll
+            for (int r = 0; r < RGW; ++r) {
+                w[2 * r] = *reinterpret_cast<const uint32_t *>(st + wo + r * 1024);
+                w[2 * r + 1] = *reinterpret_cast<const uint32_t *>(st + wo + r * 1024 + 512);
+            }
+            // the values are in registers: the slot may be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            return true;
+        };
+        if (nst > 0) ok = ok && fetch(0, wc, xc);
+        for (int s = 0; ok && s < nst; ++s) {
             const int kcol = k0 + s * kStageK + cw * 64;
             uint32_t sc[RGW];
 #pragma unroll
@@ -342,34 +376,19 @@ __global__ void __launch_bounds__(kThreads, 2)
                 for (int r = 0; r < RGW; ++r) sc[r] = scn[r];
                 load_sc(kcol + kStageK);  // next stage's column, in flight during this one
             }
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (s / a.ws) & 1, lim))) {
-                if (lane == 0) give_up();
-                ok = false;
-                break;
-            }
-            if (*abort_flag) {
+            if (s + 1 < nst && !fetch(s + 1, wn, xn)) {
                 ok = false;
                 break;
             }
             if (kcol < k1) {
-                const uint8_t *st = ring + (size_t)slot * STRIDE;
                 uint32_t b[NT8][4][2];
 #pragma unroll
-                for (int t = 0; t < NT8; ++t) {
-                    const uint4 lo = lds128(st + xo_lo + t * 8 * 128);
-                    const uint4 hi = lds128(st + xo_hi + t * 8 * 128);
-                    x_frag(lo, hi, b[t]);
-                }
+                for (int t = 0; t < NT8; ++t) x_frag(xc[t][0], xc[t][1], b[t]);
                 uint32_t zlo[RGW], zhi[RGW];
 #pragma unroll
                 for (int r = 0; r < RGW; ++r) {
-                    zlo[r] = *reinterpret_cast<const uint32_t *>(st + wo + r * 1024);
-                    zhi[r] = *reinterpret_cast<const uint32_t *>(st + wo + r * 1024 + 512);
-                }
-#pragma unroll
-                for (int r = 0; r < RGW; ++r) {
-                    zlo[r] = sign_nz(zlo[r]);
-                    zhi[r] = sign_nz(zhi[r]);
+                    zlo[r] = sign_nz(wc[2 * r]);
+                    zhi[r] = sign_nz(wc[2 * r + 1]);
                 }
                 if constexpr (GROUP) {
 #pragma unroll
@@ -411,8 +430,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+#pragma unroll
+            for (int q = 0; q < 2 * RGW; ++q) wc[q] = wn[q];
+#pragma unroll
+            for (int t = 0; t < NT8; ++t) {
+                xc[t][0] = xn[t][0];
+                xc[t][1] = xn[t][1];
+            }
         }
     }
 
@@ -617,13 +641,15 @@ cudaError_t launch_one(const GemvArgs &a, const GemvPlan &p, cudaStream_t st, bo
 // one instantiation per row-group count per warp (GemvPlan::rg = 2 * RGW row groups per CTA)
 template <int NT8, bool BF, bool GROUP, bool SILU>
 cudaError_t launch_rgw(const GemvArgs &a, const GemvPlan &p, cudaStream_t st, bool pdl) {
+    constexpr int hi = rgw_max(NT8, GROUP);
     switch (p.rg / 2) {
     case 1: return launch_one<NT8, 1, BF, GROUP, SILU>(a, p, st, pdl);
-    case 2: return launch_one<NT8, 2, BF, GROUP, SILU>(a, p, st, pdl);
-    case 3: return launch_one<NT8, 3, BF, GROUP, SILU>(a, p, st, pdl);
-    case 4: return launch_one<NT8, 4, BF, GROUP, SILU>(a, p, st, pdl);
-    default: return cudaErrorInvalidValue;
+    case 2: if constexpr (hi >= 2) return launch_one<NT8, 2, BF, GROUP, SILU>(a, p, st, pdl); break;
+    case 3: if constexpr (hi >= 3) return launch_one<NT8, 3, BF, GROUP, SILU>(a, p, st, pdl); break;
+    case 4: if constexpr (hi >= 4) return launch_one<NT8, 4, BF, GROUP, SILU>(a, p, st, pdl); break;
+    default: break;
     }
+    return cudaErrorInvalidValue;
 }
 
 template <bool BF, bool SILU>

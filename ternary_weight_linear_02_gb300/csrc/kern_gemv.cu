@@ -73,9 +73,8 @@ GemvPlan plan_gemv(int64_t M, int64_t rows, int64_t K, int sm_count, bool gated,
     const double stage_fixed = 250.0, per_rg = p.nt8 == 1 ? 90.0 : 150.0;
     double best = 1e300;
     int64_t best_ctas = 0;
-    // group-scale kernels with two token tiles hold twice the partials: <= 2 row groups a warp
-    const int rgw_max = (group && p.nt8 == 2) ? 2 : gemv::kRgwMax;
-    for (int rgw = 1; rgw <= rgw_max; ++rgw) {
+    const int rgw_hi = gemv::rgw_max(p.nt8, group);
+    for (int rgw = 1; rgw <= rgw_hi; ++rgw) {
         const int64_t RB = 32 * rgw;
         const int64_t tiles = gated ? (rows / 2 + RB / 2 - 1) / (RB / 2) : (rows + RB - 1) / RB;
         for (int sk = 1; sk <= 8; ++sk) {
@@ -86,10 +85,14 @@ GemvPlan plan_gemv(int64_t M, int64_t rows, int64_t K, int sm_count, bool gated,
             if (skr != sk && force_sk <= 0) continue;  // the same split as a smaller sk
             const int64_t ctas = tiles * skr;
             const int64_t cap = cluster_capacity((int)skr, sm_count);
-            const int64_t waves = (ctas + cap - 1) / cap;
+            // CTAs on the busiest SM over the call; two resident CTAs share an SM at
+            // ~1.5x the throughput of one (measured), so n > 1 of them take ~2n/3 of
+            // one CTA's time each
+            const int64_t n = (ctas + cap - 1) / cap;
+            const double waves = n <= 1 ? 1.0 : 0.667 * (double)n;
             const double busiest = (double)spc * (stage_fixed + per_rg * rgw);
             const double over = 1000.0 + (skr > 1 ? 1000.0 : 0.0);
-            const double cost = (double)waves * (busiest + over);
+            const double cost = waves * (busiest + over);
             if (cost < best * (1 - 1e-9) || (cost <= best * (1 + 1e-9) && ctas < best_ctas)) {
                 best = cost;
                 best_ctas = ctas;
