@@ -52,6 +52,8 @@ def _load():
         lib.oracle_linear_f64.restype = ctypes.c_int
         lib.oracle_silu_mul_f64.argtypes = [p, p, p, i64, p, i64, i64, i64, ctypes.c_int]
         lib.oracle_silu_mul_f64.restype = ctypes.c_int
+        lib.oracle_block_mask.argtypes = [p, i64, i64, p]
+        lib.oracle_block_mask.restype = i64
         _lib = lib
     return _lib
 
@@ -166,3 +168,16 @@ def silu_mul_from_bits(x_bits: np.ndarray, x_dtype: str, packed: np.ndarray,
     """Same as silu_mul_f64, taking x and the fp16 scale as raw 16-bit patterns."""
     return silu_mul_f64(bits_to_f64(x_bits, x_dtype), packed, f16_bits_to_f64(scale_bits),
                         group_size, nthreads)
+
+
+def block_mask(packed: np.ndarray) -> tuple[np.ndarray, int]:
+    """Zero-block map of packed [N, K/4]: uint32 [ceil(N/128), ceil(K/64/32)], bit kb of
+    row block rb set when rows [128 rb, +128) x k [64 kb, +64) hold a non-zero weight;
+    and the number of zero blocks."""
+    packed = np.ascontiguousarray(packed, dtype=np.uint8)
+    N, Kq = packed.shape
+    K = 4 * Kq
+    RB, KB = (N + 127) // 128, (K + 63) // 64
+    mask = np.empty((RB, (KB + 31) // 32), dtype=np.uint32)
+    zero = _load().oracle_block_mask(_ptr(packed), N, K, _ptr(mask))
+    return mask, int(zero)

@@ -219,3 +219,37 @@ int oracle_silu_mul_f64(const double *x, const uint8_t *packed, const double *sc
     free(y);
     return rc;
 }
+
+/*
+ * Zero-block map for skipping all-zero weight blocks ([P1] §6: ternary weights
+ * often come with sparse structure, and a mask of all-zero blocks lets the
+ * kernel skip them).  Block (rb, kb) covers rows [128*rb, 128*rb + 128) and
+ * weights k in [64*kb, 64*kb + 64), clipped to [0, N) x [0, K).  Its bit is 1
+ * when any weight in it decodes to a non-zero value with the code table above
+ * (so a block of 00 and 11 codes only is a zero block).
+ *   mask: uint32 [ceil(N/128)][ceil(ceil(K/64)/32)], bit kb%32 of word kb/32.
+ * Returns the number of zero blocks.
+ */
+int64_t oracle_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t *mask)
+{
+    const int64_t RB = (N + 127) / 128, KB = (K + 63) / 64, W = (KB + 31) / 32;
+    int64_t zero = 0;
+    for (int64_t i = 0; i < RB * W; ++i) mask[i] = 0u;
+    for (int64_t rb = 0; rb < RB; ++rb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            int live = 0;
+            for (int64_t n = 128 * rb; n < 128 * rb + 128 && n < N && !live; ++n) {
+                const uint8_t *row = packed + n * (K / 4);
+                for (int64_t k = 64 * kb; k < 64 * kb + 64 && k < K; ++k) {
+                    if (oracle_trit(code_of(row, k)) != 0) {
+                        live = 1;
+                        break;
+                    }
+                }
+            }
+            if (live) mask[rb * W + kb / 32] |= 1u << (kb % 32);
+            else ++zero;
+        }
+    }
+    return zero;
+}

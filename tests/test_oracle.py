@@ -336,3 +336,66 @@ def test_bit_conversions_exact(oracle_mod):
         bits = t.view(torch.int16).numpy().view(np.uint16)
         got = oracle_mod.bits_to_f64(bits, name)
         assert np.array_equal(got, t.to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------------ zero-block map
+# Blocks are 128 rows x 64 k.  Expected maps below are built from where the test
+# itself put non-zero codes, by index arithmetic only (no decode).
+def _expected_map(N, K, live_cells):
+    RB, KB = (N + 127) // 128, (K + 63) // 64
+    m = np.zeros((RB, (KB + 31) // 32), dtype=np.uint32)
+    for rb, kb in live_cells:
+        m[rb, kb // 32] |= np.uint32(1 << (kb % 32))
+    return m
+
+
+def test_block_mask_empty_and_reserved(oracle_mod):
+    N, K = 300, 4160  # ragged in both: 3 row blocks, 65 k blocks
+    for byte in (0x00, 0xFF, 0xF3, 0x3C):  # fields 00 / 11 only: every weight decodes to 0
+        p = np.full((N, K // 4), byte, dtype=np.uint8)
+        m, z = oracle_mod.block_mask(p)
+        assert m.shape == (3, 3)
+        assert not m.any() and z == 3 * 65
+
+
+@pytest.mark.parametrize("code", [1, 2])
+def test_block_mask_single_weight_positions(oracle_mod, code):
+    """One +1 or -1 weight anywhere lights exactly its own block: rows 0, 127,
+    128, 255, N-1 and k 0, 63, 64, 2047, K-1 (block edges, the ragged last blocks)."""
+    N, K = 300, 4160
+    for n in (0, 127, 128, 255, N - 1):
+        for k in (0, 63, 64, 2047, K - 1):
+            p = np.zeros((N, K // 4), dtype=np.uint8)
+            p[n, k // 4] = code << (2 * (k % 4))
+            m, z = oracle_mod.block_mask(p)
+            assert np.array_equal(m, _expected_map(N, K, [(n // 128, k // 64)])), (n, k)
+            assert z == 3 * 65 - 1
+
+
+def test_block_mask_random_pattern(oracle_mod):
+    """Live blocks carry random codes with at least one non-zero weight, zero blocks
+    random 00 / 11 fields: the map is the pattern."""
+    rng = np.random.default_rng(41)
+    N, K = 520, 1920
+    RB, KB = 5, 30
+    live = rng.random((RB, KB)) < 0.7
+    fields = rng.integers(0, 4, size=(N, K), dtype=np.uint8)
+    for rb in range(RB):
+        for kb in range(KB):
+            r0, r1, k0, k1 = rb * 128, min(N, rb * 128 + 128), kb * 64, kb * 64 + 64
+            blk = fields[r0:r1, k0:k1]
+            if live[rb, kb]:
+                blk[rng.integers(0, r1 - r0), rng.integers(0, 64)] = 1 + rng.integers(0, 2)
+            else:
+                blk[...] = 3 * (blk >= 2)  # 00 or 11
+    packed = (fields[:, 0::4] | (fields[:, 1::4] << 2) | (fields[:, 2::4] << 4)
+              | (fields[:, 3::4] << 6)).astype(np.uint8)
+    m, z = oracle_mod.block_mask(packed)
+    cells = [(rb, kb) for rb in range(RB) for kb in range(KB) if live[rb, kb]]
+    assert np.array_equal(m, _expected_map(N, K, cells))
+    assert z == int((~live).sum())
+    # a second formulation: any non-zero in the unpacked block
+    t, _ = oracle_mod.unpack(packed)
+    for rb in range(RB):
+        for kb in range(KB):
+            assert bool(np.any(t[rb * 128:rb * 128 + 128, kb * 64:kb * 64 + 64])) == bool(live[rb, kb])
