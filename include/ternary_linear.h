@@ -117,10 +117,11 @@ tl_status ternary_linear(const void *x, int32_t x_dtype, const uint8_t *packed,
 
 /* Flags for ternary_linear_ex. */
 typedef enum {
-    /* packed and scale are not written by any work still running on `stream`
-     * when this call's kernel starts (true for model weights loaded once).
-     * Lets the kernel read them before its stream predecessor has finished
-     * (programmatic dependent launch), overlapping consecutive layers. */
+    /* packed and scale (and, for the masked calls, the zero-block map) are not
+     * written by any work still running on `stream` when this call's kernel
+     * starts (true for model weights loaded once).  Lets the kernel read them
+     * before its stream predecessor has finished (programmatic dependent
+     * launch), overlapping consecutive layers. */
     TL_FLAG_STATIC_WEIGHTS = 1
 } tl_flags;
 
@@ -154,6 +155,46 @@ tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t 
                                   const void *scale, int32_t group_size, void *out,
                                   int32_t out_dtype, int64_t M, int64_t N, int64_t K,
                                   uint32_t flags, void *stream);
+
+/*
+ * Zero-block map -- skipping all-zero weight blocks ("三元量化模型接入vLLM…完整实战"
+ * §6: ternary weights often come with sparse structure; a mask of zero blocks
+ * lets the kernel skip them).
+ *
+ * ternary_block_mask -- build the map of packed [N, K/4]: block (rb, kb) covers
+ *   rows [128*rb, 128*rb + 128) and weights k in [64*kb, 64*kb + 64), clipped to
+ *   the matrix; its bit (bit kb%32 of word mask[rb * W + kb/32], W =
+ *   ceil(ceil(K/64) / 32)) is 1 when any weight in it decodes to a non-zero value
+ *   (a block of 00 and 11 codes is a zero block).  mask: device uint32
+ *   [ternary_block_mask_words(N, K)], written entirely.  zero_blocks: device
+ *   int64, may be NULL; reset on `stream`, then the number of zero blocks is
+ *   added.  Requires K % 4 == 0; reads the packed matrix once (HBM-bound).
+ *   Errors: TL_ERR_SHAPE, TL_ERR_NULL, TL_ERR_ALIGN (mask not 4-byte or count
+ *   not 8-byte aligned), TL_ERR_CUDA.  Asynchronous on stream.
+ */
+int64_t ternary_block_mask_words(int64_t N, int64_t K);  /* -1 for invalid sizes */
+tl_status ternary_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t *mask,
+                             int64_t *zero_blocks, void *stream);
+
+/*
+ * ternary_linear_masked / ternary_linear_silu_mul_masked -- ternary_linear and
+ * ternary_linear_silu_mul (same arguments, TL_PATH_AUTO) that read the zero-block
+ * map `mask` of the same packed matrix (for the gated call: of all 2N stacked
+ * rows) and neither load nor multiply blocks whose bit is 0.  The result equals
+ * the unmasked call's bit for bit when the map is the one ternary_block_mask
+ * built (a zero bit is the caller's promise that the block's weights are zero).
+ * Decode shapes (M <= 16) run on the decode kernel, the rest on the tile kernel.
+ * mask: device, 4-byte aligned, NULL only when nothing is computed.
+ */
+tl_status ternary_linear_masked(const void *x, int32_t x_dtype, const uint8_t *packed,
+                                const void *scale, int32_t group_size, const uint32_t *mask,
+                                void *out, int32_t out_dtype, int64_t M, int64_t N, int64_t K,
+                                uint32_t flags, void *stream);
+tl_status ternary_linear_silu_mul_masked(const void *x, int32_t x_dtype, const uint8_t *packed,
+                                         const void *scale, int32_t group_size,
+                                         const uint32_t *mask, void *out, int32_t out_dtype,
+                                         int64_t M, int64_t N, int64_t K, uint32_t flags,
+                                         void *stream);
 
 /* Kernels by M (TL_PATH_AUTO): M <= 16 -> the decode kernel (register-fed warp
  * MMAs, TMA-staged weights); 17 <= M <= 32 -> the tcgen05 skinny kernel (64-wide

@@ -18,7 +18,8 @@ import os
 import torch
 
 __all__ = [
-    "TernaryError", "build", "library_path", "load", "pack", "unpack", "linear", "linear_fused",
+    "TernaryError", "build", "library_path", "load", "pack", "unpack", "block_mask", "linear",
+    "linear_fused",
     "linear_silu_mul",
     "device_status", "device_status_async", "status_string", "skinny_max_m", "PATHS",
 ]
@@ -82,6 +83,16 @@ def load():
     lib.ternary_test_set_wait_limit.restype = None
     lib.ternary_device_status_async.argtypes = [p, i32, p]
     lib.ternary_device_status_async.restype = ctypes.c_int
+    lib.ternary_block_mask_words.argtypes = [i64, i64]
+    lib.ternary_block_mask_words.restype = i64
+    lib.ternary_block_mask.argtypes = [p, i64, i64, p, p, p]
+    lib.ternary_block_mask.restype = ctypes.c_int
+    lib.ternary_linear_masked.argtypes = [p, i32, p, p, i32, p, p, i32, i64, i64, i64,
+                                          ctypes.c_uint32, p]
+    lib.ternary_linear_masked.restype = ctypes.c_int
+    lib.ternary_linear_silu_mul_masked.argtypes = [p, i32, p, p, i32, p, p, i32, i64, i64, i64,
+                                                   ctypes.c_uint32, p]
+    lib.ternary_linear_silu_mul_masked.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -144,10 +155,30 @@ def unpack(packed: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
     return t, cnt
 
 
+def block_mask(packed: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    """Zero-block map of packed [N, K/4]: (mask uint32 [ceil(N/128), W], number of
+    zero blocks (device int64)); bit kb of row block rb is set when rows
+    [128 rb, +128) x k [64 kb, +64) hold a non-zero weight."""
+    _need_cuda(packed)
+    if packed.dtype != torch.uint8 or packed.dim() != 2:
+        raise ValueError("packed must be a 2-D uint8 tensor")
+    packed = packed.contiguous()
+    N, Kq = packed.shape
+    lib = load()
+    words = int(lib.ternary_block_mask_words(N, 4 * Kq))
+    rb = (N + 127) // 128
+    mask = torch.empty((rb, words // max(rb, 1) if rb else 0), dtype=torch.int32,
+                       device=packed.device)
+    cnt = torch.empty((), dtype=torch.int64, device=packed.device)
+    _check(lib.ternary_block_mask(_ptr(packed), N, 4 * Kq, _ptr(mask), _ptr(cnt),
+                                  _stream(packed.device)), "ternary_block_mask")
+    return mask, cnt
+
+
 def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
            group_size: int | None = None, out_dtype: torch.dtype | None = None,
            out: torch.Tensor | None = None, path: str = "auto",
-           static_weights: bool = False) -> torch.Tensor:
+           static_weights: bool = False, mask: torch.Tensor | None = None) -> torch.Tensor:
     """out[..., N] = x[..., K] @ (t * scale)^T with t decoded from ``packed``.
 
     ``scale`` is fp16 [N] (per channel) or [N, K/128] (per 128-wide K group);
@@ -155,7 +186,8 @@ def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
     flattened into M (the kernel takes a dense 2-D [M, K]).
     ``static_weights=True`` promises that ``packed`` / ``scale`` are not being
     written by work still running on the stream (TL_FLAG_STATIC_WEIGHTS), which
-    lets consecutive layers overlap.
+    lets consecutive layers overlap.  ``mask`` (from ``block_mask(packed)``)
+    makes the kernel skip all-zero weight blocks (automatic path only).
     """
     _need_cuda(x, packed, scale, out)
     if x.dtype not in (torch.float16, torch.bfloat16):
@@ -186,6 +218,17 @@ def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
     packed = packed.contiguous()
     scale = scale.contiguous()
     lib = load()
+    if mask is not None:
+        if path != "auto":
+            raise ValueError("a zero-block mask runs on the automatic path only")
+        _need_cuda(mask)
+        rc = lib.ternary_linear_masked(_ptr(x2), _DT[x.dtype], _ptr(packed), _ptr(scale),
+                                       int(group_size), _ptr(mask.contiguous()), _ptr(out),
+                                       _DT[odt], M, N, K,
+                                       FLAG_STATIC_WEIGHTS if static_weights else 0,
+                                       _stream(x.device))
+        _check(rc, "ternary_linear_masked")
+        return out.reshape(*lead, N)
     rc = lib.ternary_linear_ex(_ptr(x2), _DT[x.dtype], _ptr(packed), _ptr(scale),
                                int(group_size), _ptr(out), _DT[odt], M, N, K, PATHS[path],
                                FLAG_STATIC_WEIGHTS if static_weights else 0, _stream(x.device))
@@ -230,7 +273,7 @@ def device_status_async(dst: torch.Tensor, clear: bool = True) -> torch.Tensor:
 def linear_silu_mul(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
                     group_size: int | None = None, out_dtype: torch.dtype | None = None,
                     out: torch.Tensor | None = None,
-                    static_weights: bool = False) -> torch.Tensor:
+                    static_weights: bool = False, mask: torch.Tensor | None = None) -> torch.Tensor:
     """silu(g) * u for a fused gate/up layer, in one kernel.
 
     ``packed`` [2N, K/4] and ``scale`` ([2N] or [2N, K/G]) stack the gate rows
@@ -265,6 +308,16 @@ def linear_silu_mul(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
         raise ValueError("out must be a contiguous [M, N] tensor of out_dtype")
     packed = packed.contiguous()
     scale = scale.contiguous()
+    if mask is not None:
+        _need_cuda(mask)
+        rc = load().ternary_linear_silu_mul_masked(_ptr(x2), _DT[x.dtype], _ptr(packed),
+                                                   _ptr(scale), int(group_size),
+                                                   _ptr(mask.contiguous()), _ptr(out), _DT[odt],
+                                                   M, N, K,
+                                                   FLAG_STATIC_WEIGHTS if static_weights else 0,
+                                                   _stream(x.device))
+        _check(rc, "ternary_linear_silu_mul_masked")
+        return out.reshape(*lead, N)
     rc = load().ternary_linear_silu_mul(_ptr(x2), _DT[x.dtype], _ptr(packed), _ptr(scale),
                                         int(group_size), _ptr(out), _DT[odt], M, N, K,
                                         FLAG_STATIC_WEIGHTS if static_weights else 0,

@@ -180,7 +180,8 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
 
 tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
                      int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
-                     int64_t K, int32_t path, uint32_t flags, void *stream) {
+                     int64_t K, int32_t path, uint32_t flags, void *stream,
+                     const uint32_t *mask = nullptr) {
     bool noop = false;
     tl_status s = check_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
                                &noop);
@@ -209,11 +210,12 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
         gp = tl::plan_gemv(M, N, K, d->sm_count, false, group, force_sk);
     tl::SkinnyTcPlan tp{};
     tl::SkinnyPlan mp{};
-    if (!gp.ok && !g64 && impl != kImplMma) {
+    // the zero-block map is read by the decode kernel and the tile kernel only
+    if (!gp.ok && !g64 && impl != kImplMma && mask == nullptr) {
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
     }
-    if (!g64 && impl == kImplMma) mp = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
+    if (!g64 && impl == kImplMma && mask == nullptr) mp = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
     const bool skinny_ok = gp.ok || tp.ok || mp.ok;
     int use = path;
     if (use == TL_PATH_AUTO) {
@@ -237,6 +239,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
             a.odt = out_dtype;
             a.status = d->status;
             a.wait_limit = wait_limit();
+            a.mask = mask;
+            a.mask_words = tl::mask_words(K);
             return from_cuda(tl::launch_gemv(a, bf, group, gp, st, pdl_enabled()));
         }
         if (tp.ok) {
@@ -277,6 +281,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     a.K = (int)K;
     a.gshift = gshift;
     a.status = d->status;
+    a.mask = mask;
+    a.mask_words = tl::mask_words(K);
     return from_cuda(tl::launch_tile(a, bf, group, out_dtype, d->sm_count, st, pdl_enabled()));
 }
 
@@ -285,7 +291,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
 // kernel, larger M (and 64-wide groups) on the tile kernel.
 tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
                        int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
-                       int64_t K, uint32_t flags, void *stream) {
+                       int64_t K, uint32_t flags, void *stream, const uint32_t *mask = nullptr) {
     if (N < 0 || N >= ((int64_t)1 << 29)) return TL_ERR_SHAPE;
     bool noop = false;
     tl_status s = check_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, 2 * N, K,
@@ -320,10 +326,12 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
             a.odt = out_dtype;
             a.status = d->status;
             a.wait_limit = wait_limit();
+            a.mask = mask;
+            a.mask_words = tl::mask_words(K);
             return from_cuda(tl::launch_gemv_silu(a, bf, group, gp, st, pdl_enabled()));
         }
     }
-    if (M <= skinny_max_m() && group_size != 64) {
+    if (M <= skinny_max_m() && group_size != 64 && mask == nullptr) {
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, 2 * N, K, d->sm_count, force_sk, per_sm);
         if (tp.ok) {
@@ -354,6 +362,8 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     a.nh = (int)N;
     a.gshift = gshift;
     a.status = d->status;
+    a.mask = mask;
+    a.mask_words = tl::mask_words(K);
     return from_cuda(tl::launch_tile_silu(a, bf, group, out_dtype, st, pdl_enabled()));
 }
 
@@ -432,6 +442,54 @@ tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t 
                                   uint32_t flags, void *stream) {
     return run_silu_mul(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K, flags,
                         stream);
+}
+
+int64_t ternary_block_mask_words(int64_t N, int64_t K) {
+    if (N < 0 || K < 0 || K % 4 != 0) return -1;
+    return ((N + 127) / 128) * (int64_t)tl::mask_words(K);
+}
+
+tl_status ternary_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t *mask,
+                             int64_t *zero_blocks, void *stream) {
+    if (N < 0 || K < 0 || K % 4 != 0) return TL_ERR_SHAPE;
+    if (N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return TL_ERR_SHAPE;
+    if (N * K > 0 && (packed == nullptr || mask == nullptr)) return TL_ERR_NULL;
+    if ((mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) ||
+        (zero_blocks && (reinterpret_cast<uintptr_t>(zero_blocks) & 7u)))
+        return TL_ERR_ALIGN;
+    if (take_injected_failure()) return TL_ERR_CUDA;
+    DevInfo *d = nullptr;
+    tl_status s = current_device(&d, false);
+    if (s != TL_OK) return s;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (zero_blocks) {
+        s = from_cuda(cudaMemsetAsync(zero_blocks, 0, sizeof(int64_t), st));
+        if (s != TL_OK) return s;
+    }
+    if (N * K == 0) return TL_OK;
+    return from_cuda(tl::launch_block_mask(packed, N, K, mask,
+                                           reinterpret_cast<unsigned long long *>(zero_blocks), st));
+}
+
+tl_status ternary_linear_masked(const void *x, int32_t x_dtype, const uint8_t *packed,
+                                const void *scale, int32_t group_size, const uint32_t *mask,
+                                void *out, int32_t out_dtype, int64_t M, int64_t N, int64_t K,
+                                uint32_t flags, void *stream) {
+    if (mask == nullptr && M > 0 && N > 0 && K > 0) return TL_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(mask) & 3u) return TL_ERR_ALIGN;
+    return run_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
+                      TL_PATH_AUTO, flags, stream, mask);
+}
+
+tl_status ternary_linear_silu_mul_masked(const void *x, int32_t x_dtype, const uint8_t *packed,
+                                         const void *scale, int32_t group_size,
+                                         const uint32_t *mask, void *out, int32_t out_dtype,
+                                         int64_t M, int64_t N, int64_t K, uint32_t flags,
+                                         void *stream) {
+    if (mask == nullptr && M > 0 && N > 0 && K > 0) return TL_ERR_NULL;
+    if (reinterpret_cast<uintptr_t>(mask) & 3u) return TL_ERR_ALIGN;
+    return run_silu_mul(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K, flags,
+                        stream, mask);
 }
 
 int32_t ternary_skinny_max_m(void) { return skinny_max_m(); }

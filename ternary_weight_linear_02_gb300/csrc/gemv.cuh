@@ -248,6 +248,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         else return n0 + r;
     };
 
+    // Zero-block map (a.mask, optional): bit kb of word [rb][kb / 32] is set when
+    // rows [128 rb, +128) x k [64 kb, +64) hold a non-zero weight.  A stage whose
+    // blocks are all zero is neither loaded nor multiplied (producer and consumers
+    // walk the same live stages, so ring slots follow the count of live stages);
+    // a warp skips the decode and MMAs of a zero 64-k column.
+    auto rows_live = [&](int r0, int r1, int kb0, int nkb) -> bool {
+        if (r1 <= r0) return false;
+        for (int rb = r0 >> 7; rb <= (r1 - 1) >> 7; ++rb)
+            for (int kb = kb0; kb < kb0 + nkb; ++kb)
+                if ((__ldg(a.mask + (int64_t)rb * a.mask_words + (kb >> 5)) >> (kb & 31)) & 1u) return true;
+        return false;
+    };
+    // rows of the CTA's half h (gated: h = 0 gate rows, h = 1 up rows)
+    auto half_rows = [&](int h, int &r0, int &r1) {
+        if constexpr (SILU) {
+            r0 = (h ? a.nh : 0) + j0;
+            r1 = min(r0 + PH, (h ? 2 * a.nh : a.nh));
+        } else {
+            r0 = n0 + h * PH;
+            r1 = min(r0 + PH, a.N);
+        }
+    };
+    auto stage_live = [&](int s) -> bool {
+        if (a.mask == nullptr) return true;
+        const int kb0 = (k0 >> 6) + 4 * s;
+        int r0, r1;
+        half_rows(0, r0, r1);
+        if (rows_live(r0, r1, kb0, 4)) return true;
+        half_rows(1, r0, r1);
+        return rows_live(r0, r1, kb0, 4);
+    };
+    auto next_live = [&](int s) {
+        while (s < nst && !stage_live(s)) ++s;
+        return s;
+    };
+
     float acc[RGW][NT8][4];
 #pragma unroll
     for (int r = 0; r < RGW; ++r)
@@ -261,39 +297,41 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (lane == 0) {
             const bool static_w = (a.flags & kGemvStaticWeights) != 0;
             if (!static_w) pdl_wait();
-            auto issue_w = [&](int s) {
-                uint8_t *dst = ring + (size_t)(s % a.ws) * STRIDE + XST;
+            auto issue_w = [&](int s, int slot) {
+                uint8_t *dst = ring + (size_t)slot * STRIDE + XST;
                 const int kb = (k0 >> 2) + s * 64;  // byte column of the stage
                 if constexpr (SILU) {
-                    tc::tma_load_2d(dst, &tmw, kb, j0, &full[s % a.ws]);
-                    tc::tma_load_2d(dst + WST / 2, &tmw, kb, a.nh + j0, &full[s % a.ws]);
+                    tc::tma_load_2d(dst, &tmw, kb, j0, &full[slot]);
+                    tc::tma_load_2d(dst + WST / 2, &tmw, kb, a.nh + j0, &full[slot]);
                 } else {
-                    tc::tma_load_2d(dst, &tmw, kb, n0, &full[s % a.ws]);
+                    tc::tma_load_2d(dst, &tmw, kb, n0, &full[slot]);
                 }
             };
-            auto issue_x = [&](int s) {
-                uint8_t *dst = ring + (size_t)(s % a.ws) * STRIDE;
-                tc::tma_load_3d(dst, &tmx, 0, 0, (k0 >> 6) + s * 4, &full[s % a.ws]);
+            auto issue_x = [&](int s, int slot) {
+                uint8_t *dst = ring + (size_t)slot * STRIDE;
+                tc::tma_load_3d(dst, &tmx, 0, 0, (k0 >> 6) + s * 4, &full[slot]);
             };
-            // the first stages: weights now (static weights: before the wait), x after it
-            const int pre = nst < a.ws ? nst : a.ws;
-            for (int s = 0; s < pre; ++s) {
-                mbar_arrive_expect_tx(&full[s], (uint32_t)STRIDE);
-                issue_w(s);
+            // the first (up to ws) live stages: weights now (static weights: before
+            // the wait), x after it
+            int pre_s[kMaxStages];
+            int issued = 0, s = next_live(0);
+            for (; s < nst && issued < a.ws; s = next_live(s + 1)) {
+                mbar_arrive_expect_tx(&full[issued], (uint32_t)STRIDE);
+                issue_w(s, issued);
+                pre_s[issued++] = s;
             }
             if (static_w) pdl_wait();  // x belongs to the previous kernel until here
-            for (int s = 0; s < pre; ++s) issue_x(s);
-            int issued = pre;
+            for (int i = 0; i < issued; ++i) issue_x(pre_s[i], i);
             bool ok = true;
-            for (int s = pre; s < nst; ++s) {
-                const int slot = s % a.ws;
-                if (*abort_flag || !mbar_wait_bounded(&empty[slot], ((s / a.ws) - 1) & 1, lim)) {
+            for (; s < nst; s = next_live(s + 1)) {
+                const int slot = issued % a.ws;
+                if (*abort_flag || !mbar_wait_bounded(&empty[slot], ((issued / a.ws) - 1) & 1, lim)) {
                     ok = false;
                     break;
                 }
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)STRIDE);
-                issue_w(s);
-                issue_x(s);
+                issue_w(s, slot);
+                issue_x(s, slot);
                 ++issued;
             }
             if (!ok) give_up();
@@ -330,7 +368,6 @@ __global__ void __launch_bounds__(kThreads, 2)
                 }
             }
         };
-        load_sc(k0 + cw * 64);
         bool ok = true;
         if (a.flags & kGemvTestStall) {
             // testing aid: a wait on a barrier nothing arrives on runs out
@@ -343,9 +380,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         // latency and the barrier wait overlap the arithmetic.
         uint32_t wc[2 * RGW], wn[2 * RGW];  // code words (lo, hi per row group): current, next
         uint4 xc[NT8][2], xn[NT8][2];       // x (two 16-byte halves per token tile)
-        auto fetch = [&](int s, uint32_t (&w)[2 * RGW], uint4 (&x)[NT8][2]) -> bool {
-            const int slot = s % a.ws;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (s / a.ws) & 1, lim))) {
+        // fetch live stage number L (the L-th stage the producer issued) into registers
+        auto fetch = [&](int L, uint32_t (&w)[2 * RGW], uint4 (&x)[NT8][2]) -> bool {
+            const int slot = L % a.ws;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (L / a.ws) & 1, lim))) {
                 if (lane == 0) give_up();
                 return false;
             }
@@ -365,22 +403,28 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (lane == 0) mbar_arrive(&empty[slot]);
             return true;
         };
-        if (nst > 0) ok = ok && fetch(0, wc, xc);
-        for (int s = 0; ok && s < nst; ++s) {
+        int hr0, hr1;  // this warp's rows, for the column test of the zero-block map
+        half_rows(half, hr0, hr1);
+        int s = ok ? next_live(0) : nst, L = 0;
+        if (s < nst) load_sc(k0 + s * kStageK + cw * 64);
+        if (s < nst) ok = ok && fetch(0, wc, xc);
+        for (; ok && s < nst; ++L) {
             const int kcol = k0 + s * kStageK + cw * 64;
+            const int sn = next_live(s + 1);
             uint32_t sc[RGW];
 #pragma unroll
             for (int r = 0; r < RGW; ++r) sc[r] = 0u;
             if constexpr (GROUP) {
 #pragma unroll
                 for (int r = 0; r < RGW; ++r) sc[r] = scn[r];
-                load_sc(kcol + kStageK);  // next stage's column, in flight during this one
+                if (sn < nst) load_sc(k0 + sn * kStageK + cw * 64);  // in flight during this stage
             }
-            if (s + 1 < nst && !fetch(s + 1, wn, xn)) {
+            if (sn < nst && !fetch(L + 1, wn, xn)) {
                 ok = false;
                 break;
             }
-            if (kcol < k1) {
+            const bool col_live = a.mask == nullptr || rows_live(hr0, hr1, kcol >> 6, 1);
+            if (kcol < k1 && col_live) {
                 uint32_t b[NT8][4][2];
 #pragma unroll
                 for (int t = 0; t < NT8; ++t) x_frag(xc[t][0], xc[t][1], b[t]);
@@ -437,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 xc[t][0] = xn[t][0];
                 xc[t][1] = xn[t][1];
             }
+            s = sn;
         }
     }
 

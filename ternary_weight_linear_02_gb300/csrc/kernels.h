@@ -14,6 +14,13 @@ cudaError_t launch_unpack(const uint8_t *packed, int8_t *t, int64_t nbytes,
 cudaError_t launch_pack(const int8_t *t, uint8_t *packed, int64_t nbytes,
                         unsigned long long *invalid, int sm_count, cudaStream_t st);
 
+// ------------------------------------------------------------ zero-block map
+// bit kb%32 of word [rb][kb/32]: rows [128 rb, +128) x k [64 kb, +64) hold a non-zero weight
+constexpr int kMaskRows = 128, kMaskK = 64;
+inline int mask_words(int64_t K) { return (int)((((K + 63) / 64) + 31) / 32); }
+cudaError_t launch_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t *mask,
+                              unsigned long long *zero_count, cudaStream_t st);
+
 // ------------------------------------------------------------ skinny path
 constexpr int kSkinnyWarps = 8;            // warps per CTA
 constexpr int kSkinnyMaxCluster = 8;       // portable cluster size
@@ -111,6 +118,8 @@ struct GemvArgs {
     int odt;                 // output dtype: 0 fp16, 1 bf16, 2 fp32
     int *status;             // device status word (bounded-wait failures)
     long long wait_limit;    // give-up time of the main-loop waits, SM cycles
+    const uint32_t *mask;    // zero-block map of packed (nullptr: every block is read)
+    int mask_words;          // map words per 128-row block
 };
 
 struct GemvPlan {
@@ -143,6 +152,8 @@ struct TileArgs {
     int gshift;              // log2 of the group size G (6, 7 or 8) in group mode
     int nh;                  // SiLU-gated call: gate rows [0, nh), up rows [nh, 2 nh), out [M, nh]
     int *status;             // device status word (bounded-wait failures)
+    const uint32_t *mask;    // zero-block map of packed (nullptr: every block is read)
+    int mask_words;          // map words per 128-row block
 };
 
 bool tile_supported(int64_t M, int64_t N, int64_t K);

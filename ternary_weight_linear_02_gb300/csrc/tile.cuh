@@ -145,13 +145,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.status) atomicExch(a.status, kStatusTimeout);
     };
 
+    // Zero-block map (a.mask, optional; bit kb of word [rb][kb / 32] set when rows
+    // [128 rb, +128) x k [64 kb, +64) hold a non-zero weight): a 64-k chunk whose
+    // blocks are zero for this CTA's rows is neither loaded nor multiplied.  All
+    // three roles walk the same live chunks; stage indices and the MMA's
+    // accumulate flag follow the count of live chunks.
+    auto rows_live = [&](int r0, int r1, int kb) -> bool {
+        if (r1 <= r0) return false;
+        for (int rb = r0 >> 7; rb <= (r1 - 1) >> 7; ++rb)
+            if ((__ldg(a.mask + (int64_t)rb * a.mask_words + (kb >> 5)) >> (kb & 31)) & 1u) return true;
+        return false;
+    };
+    auto chunk_live = [&](int c) -> bool {
+        if (a.mask == nullptr) return true;
+        if constexpr (SILU)
+            return rows_live(j0, min(j0 + 64, a.nh), c) || rows_live(a.nh + j0, min(a.nh + j0 + 64, 2 * a.nh), c);
+        else
+            return rows_live(n0, min(n0 + 128, a.N), c);
+    };
+    auto next_live = [&](int c) {
+        while (c < nchunks && !chunk_live(c)) ++c;
+        return c;
+    };
+
     if (warp == 4) {
         // ---------------- TMA producer: x tiles
         if (lane == 0) {
             tc::prefetch_tmap(&tmx);
-            for (int c = 0; c < nchunks && !*abort_flag; ++c) {
-                const int s = c % kNS;
-                if (c >= kNS && !mbar_wait_bounded(&xempty[s], ((c / kNS) - 1) & 1)) {
+            int lc = 0;  // live chunks issued
+            for (int c = next_live(0); c < nchunks && !*abort_flag; c = next_live(c + 1), ++lc) {
+                const int s = lc % kNS;
+                if (lc >= kNS && !mbar_wait_bounded(&xempty[s], ((lc / kNS) - 1) & 1)) {
                     give_up();
                     break;
                 }
@@ -163,10 +187,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16(BN, BF);
-            for (int c = 0; c < nchunks; ++c) {
-                const int s = c % C::NA, xs = c % kNS;
-                if (*abort_flag || !mbar_wait_bounded(&afull[s], (c / C::NA) & 1) ||
-                    !mbar_wait_bounded(&xfull[xs], (c / kNS) & 1)) {
+            int lc = 0;  // live chunks multiplied
+            for (int c = next_live(0); c < nchunks; c = next_live(c + 1), ++lc) {
+                const int s = lc % C::NA, xs = lc % kNS;
+                if (*abort_flag || !mbar_wait_bounded(&afull[s], (lc / C::NA) & 1) ||
+                    !mbar_wait_bounded(&xfull[xs], (lc / kNS) & 1)) {
                     give_up();
                     break;
                 }
@@ -176,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < kKC / 16; ++kk) {
                     const uint64_t b = bdesc + (uint64_t)(kk * 2);  // +32 B per 16 elements
-                    tc::mma_ts(dcol, acol + kk * 8, b, idesc, (c | kk) != 0);
+                    tc::mma_ts(dcol, acol + kk * 8, b, idesc, (lc | kk) != 0);
                     if constexpr (SMODE == kSplit) tc::mma_ts(dcol, acol + 32 + kk * 8, b, idesc, 1);
                 }
                 tc::commit(&aempty[s]);
@@ -195,16 +220,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ngk = a.K >> a.gshift;  // scale groups per row (G = 64, 128 or 256)
         const uint16_t *srow = a.scale + (SMODE == kChannel ? 0 : (int64_t)(rowok ? n : 0) * ngk);
 
-        uint4 cur = rowok && nchunks > 0 ? *reinterpret_cast<const uint4 *>(prow) : make_uint4(0, 0, 0, 0);
-        uint4 nxt = rowok && nchunks > 1 ? *reinterpret_cast<const uint4 *>(prow + 16)
+        // live chunks c (current), c1 and c2 (codes loaded one and two chunks ahead)
+        int c = next_live(0);
+        int c1 = c < nchunks ? next_live(c + 1) : nchunks;
+        uint4 cur = rowok && c < nchunks ? *reinterpret_cast<const uint4 *>(prow + (size_t)c * 16)
                                          : make_uint4(0, 0, 0, 0);
+        uint4 nxt = rowok && c1 < nchunks ? *reinterpret_cast<const uint4 *>(prow + (size_t)c1 * 16)
+                                          : make_uint4(0, 0, 0, 0);
         bool ok = true;
-        for (int c = 0; c < nchunks; ++c) {
-            const int s = c % C::NA;
+        int lc = 0;  // live chunks decoded
+        for (; c < nchunks; ++lc) {
+            const int s = lc % C::NA;
             const uint4 codes = cur;
             cur = nxt;
-            if (rowok && c + 2 < nchunks)
-                nxt = *reinterpret_cast<const uint4 *>(prow + (size_t)(c + 2) * 16);
+            const int c2 = c1 < nchunks ? next_live(c1 + 1) : nchunks;
+            if (rowok && c2 < nchunks)
+                nxt = *reinterpret_cast<const uint4 *>(prow + (size_t)c2 * 16);
             uint32_t r[32];
             decode_word_adjacent(codes.x, r + 0);
             decode_word_adjacent(codes.y, r + 8);
@@ -241,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // wait results are made warp-uniform: tcgen05.st below is warp-collective
-            if (c >= C::NA) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&aempty[s], ((c / C::NA) - 1) & 1));
+            if (lc >= C::NA) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&aempty[s], ((lc / C::NA) - 1) & 1));
             if (!ok) give_up();
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
                 ok = false;
@@ -253,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[s]);
+            c = c1;
+            c1 = c2;
         }
         // ---------------- epilogue
         ok = __all_sync(0xffffffffu, ok);
@@ -276,6 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t d[32];
                 tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
                 tc::wait_ld();
+                if (lc == 0) {  // every chunk of this CTA's rows is a zero block: D was never written
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) d[q] = 0u;
+                }
                 if constexpr (SILU) {
                     float *ex = reinterpret_cast<float *>(smem);  // [32 tokens][64 pairs]
                     if (row >= 64) {

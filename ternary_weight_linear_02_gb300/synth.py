@@ -69,6 +69,23 @@ def packed_codes(N: int, K: int, seed: int, device="cpu", p_reserved: float = 0.
     return out
 
 
+def block_sparse(packed: torch.Tensor, p_zero: float, seed: int, rows: int = 128,
+                 cols: int = 64) -> torch.Tensor:
+    """A copy of packed [N, K/4] in which each block of `rows` weight rows x `cols`
+    weights is, with probability p_zero, overwritten with zero codes (00, or 11 in
+    a random half of the zeroed blocks) -- block-sparse weights for the
+    zero-block map.  Returns the copy; the drawn pattern is not returned."""
+    out = packed.clone()
+    N, Kq = out.shape
+    g = _gen(seed, "cpu")
+    RB, KB = (N + rows - 1) // rows, (4 * Kq + cols - 1) // cols
+    zero = torch.rand((RB, KB), generator=g) < p_zero
+    fill = torch.randint(0, 2, (RB, KB), generator=g)
+    for rb, kb in zero.nonzero().tolist():
+        out[rb * rows:(rb + 1) * rows, kb * cols // 4:(kb + 1) * cols // 4] = 0xFF if fill[rb, kb] else 0
+    return out
+
+
 def activations(M: int, K: int, dtype: torch.dtype, seed: int, device="cpu") -> torch.Tensor:
     """x [M, K] ~ N(0,1) rounded to fp16 / bf16."""
     dev = torch.device(device)

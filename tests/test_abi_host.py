@@ -180,3 +180,27 @@ def test_fused_shard_sizes_checked(lib):
     s = torch.ones(4, dtype=torch.float16)
     with pytest.raises(ValueError, match="shard"):
         tl.linear_fused(x, p, s, [3, 2])
+
+
+def test_block_mask_host_checks(lib):
+    p = ctypes.c_void_p
+    assert lib.ternary_block_mask_words(300, 4160) == 3 * 3
+    assert lib.ternary_block_mask_words(0, 64) == 0
+    assert lib.ternary_block_mask_words(4, 6) == -1
+    assert lib.ternary_block_mask(p(B), 4, 6, p(A), None, None) == TL_ERR_SHAPE
+    assert lib.ternary_block_mask(None, 4, 8, p(A), None, None) == TL_ERR_NULL
+    assert lib.ternary_block_mask(p(B), 4, 8, p(A + 2), None, None) == TL_ERR_ALIGN
+    assert lib.ternary_block_mask(p(B), 4, 8, p(A), p(C + 4), None) == TL_ERR_ALIGN
+
+
+def test_masked_linear_host_checks(lib):
+    v = ctypes.c_void_p
+    # NULL map with work to do; misaligned map; argument errors as the plain call
+    assert lib.ternary_linear_masked(v(A), 0, v(B), v(C), 0, None, v(D), 2, 4, 8, 128, 0,
+                                     None) == TL_ERR_NULL
+    assert lib.ternary_linear_masked(v(A), 0, v(B), v(C), 0, v(A + 2), v(D), 2, 4, 8, 128, 0,
+                                     None) == TL_ERR_ALIGN
+    assert lib.ternary_linear_masked(v(A), 0, v(B), v(C), 0, v(A), v(D), 2, 4, 8, 130, 0,
+                                     None) == TL_ERR_SHAPE
+    assert lib.ternary_linear_silu_mul_masked(v(A), 0, v(B), v(C), 32, v(A), v(D), 2, 4, 8, 128,
+                                              0, None) == TL_ERR_DTYPE
