@@ -9,7 +9,7 @@ and marshals numpy arrays.
 
 Sources: "三元量化模型接入vLLM：从逆向加载到Kernel优化的完整实战"
 (trdm.cn/news/729035) §1.1, §3.1, §4.2, and the Qwen2.5-7B ternary-in-vLLM
-write-up (m.nxbn.cn/news/169761) §2.2, §3.2, §4.2.  Each C function names the
+write-up (m.nxbn.cn/news/169761) §2.2, §2.3, §3.2, §4.2.  Each C function names the
 passage it follows.
 """
 from __future__ import annotations
@@ -88,23 +88,31 @@ def trit(code: int) -> int:
     return int(_load().oracle_trit(int(code)))
 
 
-def unpack(packed: np.ndarray) -> tuple[np.ndarray, int]:
-    """packed [N, K/4] uint8 -> (t [N, K] int8, number of reserved 11 fields)."""
+def _row_bytes(K: int) -> int:
+    return (K + 3) // 4
+
+
+def unpack(packed: np.ndarray, K: int | None = None) -> tuple[np.ndarray, int]:
+    """packed [N, ceil(K/4)] uint8 -> (t [N, K] int8, number of reserved 11 fields
+    among the K weights of each row).  K defaults to 4 * bytes per row; a smaller
+    K leaves the last byte's high fields as padding."""
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     N, Kq = packed.shape
-    t = np.empty((N, 4 * Kq), dtype=np.int8)
+    K = 4 * Kq if K is None else int(K)
+    if _row_bytes(K) != Kq:
+        raise ValueError(f"packed rows of {Kq} bytes do not hold K = {K}")
+    t = np.empty((N, K), dtype=np.int8)
     cnt = ctypes.c_int64(0)
-    _load().oracle_unpack(_ptr(packed), _ptr(t), N, 4 * Kq, ctypes.byref(cnt))
+    _load().oracle_unpack(_ptr(packed), _ptr(t), N, K, ctypes.byref(cnt))
     return t, int(cnt.value)
 
 
 def pack(t: np.ndarray) -> tuple[np.ndarray, int]:
-    """t [N, K] int8 -> (packed [N, K/4] uint8, number of entries outside {-1,0,1})."""
+    """t [N, K] int8 -> (packed [N, ceil(K/4)] uint8, number of entries outside
+    {-1,0,1}); padding fields are 00."""
     t = np.ascontiguousarray(t, dtype=np.int8)
     N, K = t.shape
-    if K % 4:
-        raise ValueError("K must be a multiple of 4")
-    packed = np.empty((N, K // 4), dtype=np.uint8)
+    packed = np.empty((N, _row_bytes(K)), dtype=np.uint8)
     invalid = _load().oracle_pack(_ptr(t), _ptr(packed), N, K)
     return packed, int(invalid)
 
@@ -113,16 +121,16 @@ def linear_f64(x: np.ndarray, packed: np.ndarray, scale: np.ndarray, group_size:
                nthreads: int = 1) -> np.ndarray:
     """y[M,N] = per-channel or per-group scaled ternary product, all in fp64.
 
-    x: [M,K] float64; packed: [N,K/4] uint8; scale: [N] (group_size 0) or
-    [N, K/group_size] float64.
+    x: [M,K] float64; packed: [N, ceil(K/4)] uint8; scale: [N] (group_size 0)
+    or [N, K/group_size] float64.
     """
     x = np.ascontiguousarray(x, dtype=np.float64)
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     scale = np.ascontiguousarray(scale, dtype=np.float64)
     M, K = x.shape
     N = packed.shape[0]
-    if packed.shape[1] * 4 != K:
-        raise ValueError("packed must be [N, K/4]")
+    if packed.shape[1] != _row_bytes(K):
+        raise ValueError("packed must be [N, ceil(K/4)]")
     want = (N,) if group_size == 0 else (N, K // group_size)
     if scale.shape != want:
         raise ValueError(f"scale shape {scale.shape} != {want}")
@@ -150,8 +158,8 @@ def silu_mul_f64(x: np.ndarray, packed: np.ndarray, scale: np.ndarray, group_siz
     scale = np.ascontiguousarray(scale, dtype=np.float64)
     M, K = x.shape
     N2 = packed.shape[0]
-    if N2 % 2 or packed.shape[1] * 4 != K:
-        raise ValueError("packed must be [2N, K/4]")
+    if N2 % 2 or packed.shape[1] != _row_bytes(K):
+        raise ValueError("packed must be [2N, ceil(K/4)]")
     want = (N2,) if group_size == 0 else (N2, K // group_size)
     if scale.shape != want:
         raise ValueError(f"scale shape {scale.shape} != {want}")
@@ -170,13 +178,15 @@ def silu_mul_from_bits(x_bits: np.ndarray, x_dtype: str, packed: np.ndarray,
                         group_size, nthreads)
 
 
-def block_mask(packed: np.ndarray) -> tuple[np.ndarray, int]:
-    """Zero-block map of packed [N, K/4]: uint32 [ceil(N/128), ceil(K/64/32)], bit kb of
-    row block rb set when rows [128 rb, +128) x k [64 kb, +64) hold a non-zero weight;
-    and the number of zero blocks."""
+def block_mask(packed: np.ndarray, K: int | None = None) -> tuple[np.ndarray, int]:
+    """Zero-block map of packed [N, ceil(K/4)]: uint32 [ceil(N/128), ceil(K/64/32)],
+    bit kb of row block rb set when rows [128 rb, +128) x k [64 kb, +64) hold a
+    non-zero weight; and the number of zero blocks.  K defaults to 4 * bytes per row."""
     packed = np.ascontiguousarray(packed, dtype=np.uint8)
     N, Kq = packed.shape
-    K = 4 * Kq
+    K = 4 * Kq if K is None else int(K)
+    if _row_bytes(K) != Kq:
+        raise ValueError(f"packed rows of {Kq} bytes do not hold K = {K}")
     RB, KB = (N + 127) // 128, (K + 63) // 64
     mask = np.empty((RB, (KB + 31) // 32), dtype=np.uint32)
     zero = _load().oracle_block_mask(_ptr(packed), N, K, _ptr(mask))

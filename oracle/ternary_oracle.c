@@ -24,6 +24,13 @@
  *          §3.2  per-output-channel scale [N] multiplies row n
  *                (scale.view(-1,1), i.e. broadcast along K)
  *          §4.2  Y[m,n] = scale[n] * sum_k t[n,k] * X[m,k]
+ *          §2.3  packing needs the input width K to be a multiple of 4; an
+ *                export whose K is not pads each row up to whole bytes, and
+ *                the padding fields must be cut off after unpacking.  Read
+ *                here as: a row of K weights takes ceil(K/4) bytes, fields
+ *                at k >= K are padding, pack writes them as 00, unpack and
+ *                every product skip them (they are not weights, so an 11
+ *                there is not counted as reserved)
  *
  * Precision: everything is fp64.  The callers convert fp16 / bf16 inputs to
  * fp64 exactly before calling in, so the only rounding here is the fp64
@@ -51,6 +58,12 @@ int oracle_trit(unsigned code)
     }
 }
 
+/* Bytes per packed row of K weights ([P2] §2.3: whole bytes, padded). */
+static int64_t row_bytes(int64_t K)
+{
+    return (K + 3) / 4;
+}
+
 /* The 2-bit code of weight k in a packed row: byte k/4, field k%4, where
  * field j occupies bits [2j+1 : 2j] ([P1] §3.1 "first weight in the lowest
  * two bits", [P2] §2.2 "from low bits to high bits"). */
@@ -61,14 +74,15 @@ static unsigned code_of(const uint8_t *row, int64_t k)
     return (byte >> (2u * field)) & 3u;
 }
 
-/* packed [N, K/4] u8 -> t [N, K] int8 in {-1,0,+1}.
- * reserved_count (nullable) receives the number of 11 fields seen. */
+/* packed [N, ceil(K/4)] u8 -> t [N, K] int8 in {-1,0,+1}.
+ * reserved_count (nullable) receives the number of 11 fields seen among the
+ * K weights of each row (padding fields are not looked at). */
 void oracle_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
                    int64_t *reserved_count)
 {
     int64_t reserved = 0;
     for (int64_t n = 0; n < N; ++n) {
-        const uint8_t *row = packed + n * (K / 4);
+        const uint8_t *row = packed + n * row_bytes(K);
         for (int64_t k = 0; k < K; ++k) {
             unsigned c = code_of(row, k);
             if (c == 3) ++reserved;
@@ -89,21 +103,25 @@ static unsigned code_for(int v, int *ok)
     return 0u;      /* an illegal value is written as 00 and counted */
 }
 
-/* t [N, K] int8 -> packed [N, K/4] u8.  Never writes the reserved code 11.
+/* t [N, K] int8 -> packed [N, ceil(K/4)] u8.  Never writes the reserved code
+ * 11; padding fields (k >= K) are written as 00.
  * Returns the number of entries outside {-1,0,+1}. */
 int64_t oracle_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K)
 {
     int64_t invalid = 0;
+    const int64_t Kq = row_bytes(K);
     for (int64_t n = 0; n < N; ++n) {
-        for (int64_t i = 0; i < K / 4; ++i) {
+        for (int64_t i = 0; i < Kq; ++i) {
             unsigned byte = 0;
             for (unsigned j = 0; j < 4; ++j) {
+                const int64_t k = 4 * i + j;
+                if (k >= K) break; /* padding: 00 */
                 int ok;
-                unsigned c = code_for(t[n * K + 4 * i + j], &ok);
+                unsigned c = code_for(t[n * K + k], &ok);
                 if (!ok) ++invalid;
                 byte |= c << (2u * j);
             }
-            packed[n * (K / 4) + i] = (uint8_t)byte;
+            packed[n * Kq + i] = (uint8_t)byte;
         }
     }
     return invalid;
@@ -118,7 +136,7 @@ int64_t oracle_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K)
  *       y[m,n] = sum_{g<K/G} s[n,g] * ( sum_{k in [gG, gG+G)} t[n,k] * x[m,k] )
  *
  * x: [M,K] fp64 row-major; scale: [N] or [N, K/G] fp64 row-major;
- * packed: [N, K/4] u8; y: [M,N] fp64 row-major.
+ * packed: [N, ceil(K/4)] u8; y: [M,N] fp64 row-major.
  */
 typedef struct {
     const double *x;
@@ -136,7 +154,7 @@ static void *linear_rows(void *arg)
     int8_t *trow = (int8_t *)malloc((size_t)(K > 0 ? K : 1));
     for (int64_t n = j->n_begin; n < j->n_end; ++n) {
         /* decode row n once with the code table */
-        oracle_unpack(j->packed + n * (K / 4), trow, 1, K, NULL);
+        oracle_unpack(j->packed + n * row_bytes(K), trow, 1, K, NULL);
         for (int64_t m = 0; m < M; ++m) {
             const double *xm = j->x + m * K;
             double y;
@@ -166,7 +184,7 @@ int oracle_linear_f64(const double *x, const uint8_t *packed, const double *scal
                       int64_t group_size, double *y, int64_t M, int64_t N,
                       int64_t K, int nthreads)
 {
-    if (M < 0 || N < 0 || K < 0 || K % 4 != 0) return -1;
+    if (M < 0 || N < 0 || K < 0) return -1;
     if (group_size < 0 || (group_size > 0 && K % group_size != 0)) return -1;
     if (nthreads < 1) nthreads = 1;
     if (nthreads > N) nthreads = (int)(N > 0 ? N : 1);
@@ -228,6 +246,8 @@ int oracle_silu_mul_f64(const double *x, const uint8_t *packed, const double *sc
  * when any weight in it decodes to a non-zero value with the code table above
  * (so a block of 00 and 11 codes only is a zero block).
  *   mask: uint32 [ceil(N/128)][ceil(ceil(K/64)/32)], bit kb%32 of word kb/32.
+ *   packed: [N, ceil(K/4)]; padding fields are not weights and never light a
+ *   block.
  * Returns the number of zero blocks.
  */
 int64_t oracle_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t *mask)
@@ -239,7 +259,7 @@ int64_t oracle_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t 
         for (int64_t kb = 0; kb < KB; ++kb) {
             int live = 0;
             for (int64_t n = 128 * rb; n < 128 * rb + 128 && n < N && !live; ++n) {
-                const uint8_t *row = packed + n * (K / 4);
+                const uint8_t *row = packed + n * row_bytes(K);
                 for (int64_t k = 64 * kb; k < 64 * kb + 64 && k < K; ++k) {
                     if (oracle_trit(code_of(row, k)) != 0) {
                         live = 1;

@@ -399,3 +399,77 @@ def test_block_mask_random_pattern(oracle_mod):
     for rb in range(RB):
         for kb in range(KB):
             assert bool(np.any(t[rb * 128:rb * 128 + 128, kb * 64:kb * 64 + 64])) == bool(live[rb, kb])
+
+
+# ---------------------------------------------------------------- K % 4 != 0
+def _tail_rows():
+    for row in read_golden("tail_rows.txt"):
+        K = int(row[0])
+        packed = np.array([[int(b, 16) for b in row[1].split(",")]], dtype=np.uint8)
+        t = np.array([[int(v) for v in row[2:]]], dtype=np.int8)
+        assert t.shape[1] == K
+        yield K, packed, t
+
+
+def test_tail_rows_pack_and_unpack_by_hand(oracle_mod):
+    for K, packed, t in _tail_rows():
+        got, invalid = oracle_mod.pack(t)
+        assert invalid == 0 and np.array_equal(got, packed), K
+        back, reserved = oracle_mod.unpack(packed, K)
+        assert reserved == 0 and np.array_equal(back, t), K
+
+
+def test_tail_padding_fields_are_not_weights(oracle_mod):
+    """Any codes in the padding fields (11 included) change neither the unpacked
+    weights, nor the reserved count, nor the product, nor the zero-block map."""
+    for K, packed, t in _tail_rows():
+        pad = 4 * packed.shape[1] - K
+        for fill in (1, 2, 3):
+            dirty = packed.copy()
+            for j in range(4 - pad, 4):
+                dirty[0, -1] |= fill << (2 * j)
+            back, reserved = oracle_mod.unpack(dirty, K)
+            assert reserved == 0 and np.array_equal(back, t), (K, fill)
+            x = 3.0 ** np.arange(K)[None, :]
+            assert np.array_equal(oracle_mod.linear_f64(x, dirty, np.ones(1), 0),
+                                  oracle_mod.linear_f64(x, packed, np.ones(1), 0))
+        zero_row = np.zeros_like(packed)
+        zero_row[0, -1] = 0xFF & ~((1 << (2 * (4 - pad))) - 1)  # padding fields all 11 / 01
+        m, z = oracle_mod.block_mask(zero_row, K)
+        assert not m.any() and z == 1
+
+
+def test_tail_balanced_ternary_every_last_byte(oracle_mod):
+    """K = 4q + r (r = 1, 2, 3): row n ends with byte n, x_k = 3^k, s = 1.  y[n]
+    is the balanced-ternary number of the row's weights: the first r fields of
+    byte n (from the golden table) times 3^(4q) -- the padding fields drop out."""
+    table = table_from_golden()
+    for K in (5, 6, 7, 9, 14):
+        q, r = divmod(K, 4)
+        packed = np.zeros((256, q + 1), dtype=np.uint8)
+        packed[:, 0] = 0x49  # 1 -1 0 1
+        packed[:, q] = np.arange(256, dtype=np.uint8)
+        x = (3.0 ** np.arange(K))[None, :]
+        y = oracle_mod.linear_f64(x, packed, np.ones(256), 0)[0]
+        for b in range(256):
+            head = 1 - 3 + 27
+            tail = sum(table[(b >> (2 * j)) & 3] * 3 ** (4 * q + j) for j in range(r))
+            assert y[b] == head + tail, (K, b)
+
+
+def test_tail_per_channel_matches_library_matmul(oracle_mod):
+    """Random K % 4 != 0 layers against numpy's matmul of the hand-decoded
+    weights (second formulation of the table, padding fields random)."""
+    rng = np.random.default_rng(23)
+    for K in (1, 2, 3, 101, 333):
+        N, M = 37, 5
+        Kq = (K + 3) // 4
+        packed = rng.integers(0, 256, size=(N, Kq), dtype=np.uint8)
+        t = second_formulation(packed)[:, :K].astype(np.float64)
+        x = rng.standard_normal((M, K))
+        s = rng.uniform(0.01, 0.1, size=N)
+        want = (x @ t.T) * s[None, :]
+        np.testing.assert_allclose(oracle_mod.linear_f64(x, packed, s, 0), want,
+                                   rtol=1e-12, atol=1e-12)
+        got_t, _ = oracle_mod.unpack(packed, K)
+        assert np.array_equal(got_t, t.astype(np.int8))
