@@ -172,18 +172,20 @@ class Workload:
                 ys.append(yr)
             self.x[M], self.y[M] = xs, ys
 
-    def run(self, tl, M):
-        """One pass of the stack at M tokens (every call with static weights)."""
+    def run(self, tl, M, masks=None):
+        """One pass of the stack at M tokens (every call with static weights);
+        masks[d][layer]: zero-block maps to skip zero blocks with."""
         cfg = self.cfg
         for d in range(cfg.depth):
             for j, c in enumerate(self.calls):
                 packed, scale = self.w[d][c.layer]
+                kw = {} if masks is None else {"mask": masks[d][c.layer]}
                 if c.kind == "silu_mul":
                     tl.linear_silu_mul(self.x[M][d][j], packed, scale, cfg.group_size,
-                                       out=self.y[M][d][j], static_weights=True)
+                                       out=self.y[M][d][j], static_weights=True, **kw)
                 else:
                     tl.linear(self.x[M][d][j], packed, scale, cfg.group_size,
-                              out=self.y[M][d][j], static_weights=True)
+                              out=self.y[M][d][j], static_weights=True, **kw)
 
     def calls_per_pass(self):
         return self.cfg.depth * len(self.calls)
@@ -384,6 +386,44 @@ def time_comparators(wl, tl, stream, reps):
     return res
 
 
+def time_sparse(tl, stream, dev, reps, p_zero=0.3, Ms=(1, 16, 256)):
+    """Zero-block skipping on block-sparse weights: the 7B stack's layer shapes
+    (6 model layers, 350 MB packed) with each 128-row x 64-k block zeroed with
+    probability p_zero, timed without and with the zero-block maps."""
+    cfg = bench_config("stack7b", depth=6)
+    wl = Workload(cfg, Ms, dev)
+    for d in range(cfg.depth):
+        for i, (p, sc) in enumerate(wl.w[d]):
+            wl.w[d][i] = (synth.block_sparse(p, p_zero, synth.seed_for("sparse", d, i) & 0xFFFFFFFF), sc)
+    masks, zero, total = [], 0, 0
+    for row in wl.w:
+        mrow = []
+        for p, _ in row:
+            m, z = tl.block_mask(p)
+            mrow.append(m)
+            zero += int(z.item())
+            total += ((p.shape[0] + 127) // 128) * ((p.shape[1] * 4 + 63) // 64)
+        masks.append(mrow)
+    for M in Ms:
+        wl.run(tl, M)
+        wl.run(tl, M, masks)
+    torch.cuda.synchronize()
+    out = {"workload": describe(cfg, Ms), "zero_block_fraction": round(zero / max(total, 1), 4),
+           "block": "128 rows x 64 k", "per_M": {}}
+    for M in Ms:
+        gd = capture(lambda M=M: wl.run(tl, M), stream)
+        gm = capture(lambda M=M: wl.run(tl, M, masks), stream)
+        _, per, _, _ = time_passes([gd, gm], stream, reps, 3, lambda: None)
+        out["per_M"][str(M)] = {"dense_us": round(per[0] / reps * 1e3, 2),
+                                "masked_us": round(per[1] / reps * 1e3, 2),
+                                "speedup": round(per[0] / per[1], 3)}
+        del gd, gm
+    del wl, masks
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def per_m_brief(cfg, M, ms):
     t = ms * 1e-3
     return {"us_per_pass": round(ms * 1e3, 2), "packed_GBps": round(packed_bytes(cfg) / t / 1e9, 1),
@@ -570,6 +610,10 @@ def main():
                   file=sys.stderr)
             dev_status = dev_status or st2
 
+    sparse = None
+    if not args.no_configs and args.workload == "stack7b" and not args.depth and world == 1:
+        sparse = time_sparse(tl, stream, dev, reps)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         v, desc, _ = oracle_sample(cfg, Ms, args.cpu_budget, threads)
@@ -594,6 +638,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": calls * len(Ms) * args.steps,
         "comparator": comparator,
+        "sparse_skip": sparse,
         "clocks": clk,
         "device_status": tl.status_string(dev_status),
     }

@@ -3,13 +3,17 @@
  * layer for NVIDIA GB300 (sm_103a).
  *
  * Format (all calls): a weight matrix W[N,K] with entries in {-1,0,+1} is
- * stored packed as uint8 [N, K/4], row-major, K contiguous.  Weight k of row n
- * is the 2-bit field (packed[n, k/4] >> 2*(k%4)) & 3 -- four weights per byte,
+ * stored packed as uint8 [N, ceil(K/4)], row-major, K contiguous (written
+ * [N, K/4] below: the two agree when K % 4 == 0).  Weight k of row n is the
+ * 2-bit field (packed[n, k/4] >> 2*(k%4)) & 3 -- four weights per byte,
  * little-endian, first weight in the lowest two bits -- with the code table
- * 00 -> 0, 01 -> +1, 10 -> -1, 11 -> reserved, read as 0.
+ * 00 -> 0, 01 -> +1, 10 -> -1, 11 -> reserved, read as 0.  When K % 4 != 0 the
+ * last byte of a row holds K % 4 weights and 4 - K % 4 padding fields, which no
+ * call reads as weights (pack writes them 00).
  *   Source: "三元量化模型接入vLLM：从逆向加载到Kernel优化的完整实战"
  *   (trdm.cn/news/729035) §2.2, §3.1; the Qwen2.5-7B ternary-in-vLLM write-up
- *   (m.nxbn.cn/news/169761) §2.1, §2.2.
+ *   (m.nxbn.cn/news/169761) §2.1, §2.2, and §2.3 for the padding (an export
+ *   pads rows to whole bytes; the padding is cut off after unpacking).
  *
  * Conventions shared by every entry point:
  *   - Pointers named in the signature are DEVICE pointers (cudaMalloc'd or
@@ -38,11 +42,10 @@ extern "C" {
 typedef enum {
     TL_OK = 0,
     TL_ERR_NULL = 1,        /* a required pointer is NULL                        */
-    TL_ERR_SHAPE = 2,       /* negative size, K % 4 != 0, K not a multiple of the
+    TL_ERR_SHAPE = 2,       /* negative size, K not a multiple of the
                                group size, or a size beyond the supported range  */
     TL_ERR_DTYPE = 3,       /* unknown dtype code or unsupported group size      */
-    TL_ERR_ALIGN = 4,       /* pointer not 16-byte aligned, or K % 64 != 0 for
-                               ternary_linear (packed rows must be 16-byte pitched) */
+    TL_ERR_ALIGN = 4,       /* pointer not 16-byte aligned                      */
     TL_ERR_VALUE = 5,       /* reserved for callers mapping a non-zero invalid /
                                reserved count to an error                        */
     TL_ERR_CUDA = 6,        /* a CUDA runtime call or a kernel launch failed     */
@@ -58,7 +61,9 @@ typedef enum { TL_F16 = 0, TL_BF16 = 1, TL_F32 = 2 } tl_dtype;
 typedef enum {
     TL_PATH_AUTO = 0,    /* skinny path for M <= ternary_skinny_max_m(), else tile */
     TL_PATH_SKINNY = 1,  /* fused decode + register-fed MMA GEMV / skinny GEMM     */
-    TL_PATH_TILE = 2     /* TMA + tcgen05 + TMEM tile GEMM                          */
+    TL_PATH_TILE = 2,    /* TMA + tcgen05 + TMEM tile GEMM                          */
+    TL_PATH_GENERIC = 3  /* CUDA-core kernel for any K (the one TL_PATH_AUTO
+                            uses when K % 64 != 0); SKINNY and TILE need K % 64 == 0 */
 } tl_path;
 
 /*
@@ -69,7 +74,8 @@ typedef enum {
  *   invalid_count: device int64, may be NULL.  When non-NULL the library sets
  *   it to zero on `stream` and then adds the number of invalid entries; read it
  *   after synchronising `stream`.
- *   Requires K % 4 == 0.  N == 0 or K == 0 enqueues only the count reset.
+ *   Any K >= 0 (padding fields of a K % 4 != 0 row are written 00).  N == 0 or
+ *   K == 0 enqueues only the count reset.
  */
 tl_status ternary_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
                        int64_t *invalid_count, void *stream);
@@ -80,7 +86,8 @@ tl_status ternary_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
  *   ("三元量化模型接入vLLM…完整实战" §3.1; Qwen2.5-7B write-up §2.2.)
  *   reserved_count: device int64, may be NULL; reset to zero on `stream`, then
  *   the number of 11 fields is added.
- *   Requires K % 4 == 0.
+ *   Any K >= 0: padding fields of a K % 4 != 0 row are neither decoded nor
+ *   counted.
  */
 tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
                          int64_t *reserved_count, void *stream);
@@ -96,6 +103,9 @@ tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
  *   group_size == 64  : the same with 64-wide groups, scale fp16 [N, K/64]
  *                       ("Bonsai 2 27B" port §4.2, §5.2); the skinny path
  *                       serves it for M <= 16, the tile kernel above
+ *   group_size == 32  : the same with 32-wide groups, scale fp16 [N, K/32]
+ *                       (the finer per-group choice of "第13章 量化：精度与速度的
+ *                       工程平衡" §13.3.3); served by the tile kernel at every M
  *   group_size == 256 : the same with 256-wide groups, scale fp16 [N, K/256]
  *                       (the coarser per-group choice of "第13章 量化：精度与速度的
  *                       工程平衡" §13.3.3); every path serves it
@@ -103,8 +113,12 @@ tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
  *   x_dtype  : TL_F16 or TL_BF16.  scale is always fp16.
  *   out_dtype: TL_F16, TL_BF16 or TL_F32.  Accumulation is fp32; a 16-bit
  *              output is rounded to nearest even from fp32.
- *   Sizes: M, N >= 0; K >= 0 with K % 64 == 0 (and K a multiple of the group
- *   size in group mode).  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *   Sizes: M, N >= 0; K >= 0 (a multiple of the group size in group mode, so
+ *   K % 4 != 0 is per-channel only).  M == 0 or N == 0 is a no-op; K == 0 writes zeros.
+ *   K % 64 != 0 (packed rows not 16-byte pitched: the Qwen2.5-7B write-up §2.3
+ *   notes input widths that do not fit the packing neatly) runs on the generic
+ *   CUDA-core kernel, whose reads need no alignment beyond the element's; the
+ *   16-byte pointer rule above still applies to every call.
  *   Fused layers (QKV, gate/up) are one call over the stacked rows: shard i
  *   occupies rows [off_i, off_i + N_i) of packed and of scale, and columns
  *   [off_i, off_i + N_i) of out.
@@ -127,8 +141,9 @@ typedef enum {
 
 /* ternary_linear with an explicit kernel path (tl_path) and tl_flags bits.
  * Returns TL_ERR_UNSUPPORTED if the forced path cannot serve the arguments
- * (the skinny path serves M <= 32), TL_ERR_DTYPE for an unknown path or
- * flag bit.  ternary_linear(...) == ternary_linear_ex(..., TL_PATH_AUTO, 0, stream). */
+ * (the skinny path serves M <= 32 with groups of 64 only for M <= 16 and no
+ * 32-wide groups; SKINNY and TILE need K % 64 == 0), TL_ERR_DTYPE for an
+ * unknown path or flag bit.  ternary_linear(...) == ternary_linear_ex(..., TL_PATH_AUTO, 0, stream). */
 tl_status ternary_linear_ex(const void *x, int32_t x_dtype, const uint8_t *packed,
                             const void *scale, int32_t group_size, void *out,
                             int32_t out_dtype, int64_t M, int64_t N, int64_t K,
@@ -142,12 +157,12 @@ tl_status ternary_linear_ex(const void *x, int32_t x_dtype, const uint8_t *packe
  *   out[m, j] = silu(g[m, j]) * u[m, j],  silu(v) = v / (1 + exp(-v)),  j < N
  * The stacked layout is the fused gate/up layer of ternary_linear (shards at
  * row offsets 0 and N; "三元量化模型接入vLLM…完整实战" §3.2).
- *   packed: [2N, K/4]; scale: fp16 [2N] (group_size 0) or [2N, K/G] (G = 64,
- *   128 or 256); out: [M, N] in out_dtype; g and u are fp32 (scaled) and the
+ *   packed: [2N, K/4]; scale: fp16 [2N] (group_size 0) or [2N, K/G] (G = 32,
+ *   64, 128 or 256); out: [M, N] in out_dtype; g and u are fp32 (scaled) and the
  *   product is computed in fp32, then rounded to out_dtype.
  *   flags: TL_FLAG_STATIC_WEIGHTS or 0.
- * Decode shapes (M <= ternary_skinny_max_m(), G != 64) run on the decode
- * kernel, the rest on the tile kernel, each with the product in its epilogue.
+ * Decode shapes run on the decode kernel, the rest on the tile kernel (K % 64
+ * != 0: the generic kernel), each with the product in its epilogue.
  * Argument errors as ternary_linear (with 2N rows).  N == 0 or M == 0 is a
  * no-op; K == 0 writes zeros.  Asynchronous on stream.
  */
@@ -168,7 +183,8 @@ tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t 
  *   (a block of 00 and 11 codes is a zero block).  mask: device uint32
  *   [ternary_block_mask_words(N, K)], written entirely.  zero_blocks: device
  *   int64, may be NULL; reset on `stream`, then the number of zero blocks is
- *   added.  Requires K % 4 == 0; reads the packed matrix once (HBM-bound).
+ *   added.  Any K >= 0 (padding fields never light a block); reads the
+ *   packed matrix once (HBM-bound).
  *   Errors: TL_ERR_SHAPE, TL_ERR_NULL, TL_ERR_ALIGN (mask not 4-byte or count
  *   not 8-byte aligned), TL_ERR_CUDA.  Asynchronous on stream.
  */
@@ -196,9 +212,12 @@ tl_status ternary_linear_silu_mul_masked(const void *x, int32_t x_dtype, const u
                                          int64_t M, int64_t N, int64_t K, uint32_t flags,
                                          void *stream);
 
-/* Kernels by M (TL_PATH_AUTO): M <= 16 -> the decode kernel (register-fed warp
- * MMAs, TMA-staged weights); 17 <= M <= 32 -> the tcgen05 skinny kernel (64-wide
- * groups: tile kernel); larger M -> the tcgen05 tile kernel. */
+/* Kernels by M (TL_PATH_AUTO, K % 64 == 0): M <= 16 -> the decode kernel
+ * (register-fed warp MMAs, TMA-staged weights); 17 <= M <= 32 -> the tcgen05
+ * skinny kernel (64-wide groups: tile kernel); larger M -> the tcgen05 tile
+ * kernel.  32-wide groups run on the tile kernel at every M; K % 64 != 0 runs
+ * on the generic kernel at every M, which reads no zero-block map (the masked
+ * calls then equal the unmasked ones trivially). */
 
 /* Largest M the automatic dispatch sends to the skinny path (default 32,
  * overridable with the environment variable TERNARY_SKINNY_MAX_M, read once). */

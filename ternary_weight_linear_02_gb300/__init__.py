@@ -19,6 +19,7 @@ import torch
 
 __all__ = [
     "TernaryError", "build", "library_path", "load", "pack", "unpack", "block_mask", "linear",
+    "row_bytes",
     "linear_fused",
     "linear_silu_mul",
     "device_status", "device_status_async", "status_string", "skinny_max_m", "PATHS",
@@ -29,7 +30,7 @@ _LIB_PATH = os.path.join(_PKG, "libternary_gb300.so")
 _lib = None
 
 TL_F16, TL_BF16, TL_F32 = 0, 1, 2
-PATHS = {"auto": 0, "skinny": 1, "tile": 2}
+PATHS = {"auto": 0, "skinny": 1, "tile": 2, "generic": 3}
 FLAG_STATIC_WEIGHTS = 1
 _DT = {torch.float16: TL_F16, torch.bfloat16: TL_BF16, torch.float32: TL_F32}
 
@@ -127,50 +128,69 @@ def _need_cuda(*ts):
             raise ValueError("tensors must be on a CUDA device (no CPU path)")
 
 
+def row_bytes(K: int) -> int:
+    """Bytes per packed row of K weights: ceil(K/4) (a K % 4 != 0 row ends in
+    padding fields)."""
+    return (int(K) + 3) // 4
+
+
 def pack(t: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """t [N,K] int8 in {-1,0,1} -> (packed [N,K/4] uint8, invalid-entry count (device int64))."""
+    """t [N,K] int8 in {-1,0,1} -> (packed [N, ceil(K/4)] uint8, invalid-entry count
+    (device int64)); padding fields of a K % 4 != 0 row are written 00."""
     _need_cuda(t)
     if t.dtype != torch.int8 or t.dim() != 2:
         raise ValueError("t must be a 2-D int8 tensor")
     t = t.contiguous()
     N, K = t.shape
-    packed = torch.empty((N, K // 4), dtype=torch.uint8, device=t.device)
+    packed = torch.empty((N, row_bytes(K)), dtype=torch.uint8, device=t.device)
     cnt = torch.empty((), dtype=torch.int64, device=t.device)
     _check(load().ternary_pack(_ptr(t), _ptr(packed), N, K, _ptr(cnt), _stream(t.device)),
            "ternary_pack")
     return packed, cnt
 
 
-def unpack(packed: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """packed [N,K/4] uint8 -> (t [N,K] int8, reserved-code count (device int64))."""
+def _row_width(packed: torch.Tensor, K: int | None) -> int:
+    Kq = packed.shape[1]
+    K = 4 * Kq if K is None else int(K)
+    if row_bytes(K) != Kq:
+        raise ValueError(f"packed rows of {Kq} bytes do not hold K = {K}")
+    return K
+
+
+def unpack(packed: torch.Tensor, K: int | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """packed [N, ceil(K/4)] uint8 -> (t [N,K] int8, reserved-code count (device
+    int64)).  K defaults to 4 * bytes per row; a smaller K drops the padding fields."""
     _need_cuda(packed)
     if packed.dtype != torch.uint8 or packed.dim() != 2:
         raise ValueError("packed must be a 2-D uint8 tensor")
     packed = packed.contiguous()
-    N, Kq = packed.shape
-    t = torch.empty((N, 4 * Kq), dtype=torch.int8, device=packed.device)
+    N = packed.shape[0]
+    K = _row_width(packed, K)
+    t = torch.empty((N, K), dtype=torch.int8, device=packed.device)
     cnt = torch.empty((), dtype=torch.int64, device=packed.device)
-    _check(load().ternary_unpack(_ptr(packed), _ptr(t), N, 4 * Kq, _ptr(cnt),
+    _check(load().ternary_unpack(_ptr(packed), _ptr(t), N, K, _ptr(cnt),
                                  _stream(packed.device)), "ternary_unpack")
     return t, cnt
 
 
-def block_mask(packed: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
-    """Zero-block map of packed [N, K/4]: (mask uint32 [ceil(N/128), W], number of
-    zero blocks (device int64)); bit kb of row block rb is set when rows
-    [128 rb, +128) x k [64 kb, +64) hold a non-zero weight."""
+def block_mask(packed: torch.Tensor, K: int | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """Zero-block map of packed [N, ceil(K/4)]: (mask uint32 [ceil(N/128), W], number
+    of zero blocks (device int64)); bit kb of row block rb is set when rows
+    [128 rb, +128) x k [64 kb, +64) hold a non-zero weight.  K defaults to
+    4 * bytes per row."""
     _need_cuda(packed)
     if packed.dtype != torch.uint8 or packed.dim() != 2:
         raise ValueError("packed must be a 2-D uint8 tensor")
     packed = packed.contiguous()
-    N, Kq = packed.shape
+    N = packed.shape[0]
+    K = _row_width(packed, K)
     lib = load()
-    words = int(lib.ternary_block_mask_words(N, 4 * Kq))
+    words = int(lib.ternary_block_mask_words(N, K))
     rb = (N + 127) // 128
     mask = torch.empty((rb, words // max(rb, 1) if rb else 0), dtype=torch.int32,
                        device=packed.device)
     cnt = torch.empty((), dtype=torch.int64, device=packed.device)
-    _check(lib.ternary_block_mask(_ptr(packed), N, 4 * Kq, _ptr(mask), _ptr(cnt),
+    _check(lib.ternary_block_mask(_ptr(packed), N, K, _ptr(mask), _ptr(cnt),
                                   _stream(packed.device)), "ternary_block_mask")
     return mask, cnt
 
@@ -181,8 +201,10 @@ def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
            static_weights: bool = False, mask: torch.Tensor | None = None) -> torch.Tensor:
     """out[..., N] = x[..., K] @ (t * scale)^T with t decoded from ``packed``.
 
-    ``scale`` is fp16 [N] (per channel) or [N, K/128] (per 128-wide K group);
-    ``group_size`` defaults from its rank.  Leading dimensions of ``x`` are
+    ``scale`` is fp16 [N] (per channel) or [N, K/G] (per G-wide K group, G in
+    32, 64, 128, 256); ``group_size`` defaults from its shape.  ``path`` is
+    "auto", "skinny", "tile" or "generic" (the CUDA-core kernel that "auto"
+    takes when K % 64 != 0).  Leading dimensions of ``x`` are
     flattened into M (the kernel takes a dense 2-D [M, K]).
     ``static_weights=True`` promises that ``packed`` / ``scale`` are not being
     written by work still running on the stream (TL_FLAG_STATIC_WEIGHTS), which
@@ -203,8 +225,8 @@ def linear(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
         M *= int(d)
     x2 = x.reshape(M, K).contiguous()
     N = packed.shape[0]
-    if packed.shape[1] * 4 != K:
-        raise ValueError(f"packed is [N, {packed.shape[1]}] but K/4 = {K / 4}")
+    if packed.shape[1] != row_bytes(K):
+        raise ValueError(f"packed is [N, {packed.shape[1]}] but ceil(K/4) = {row_bytes(K)}")
     if group_size is None:
         group_size = 0 if scale.dim() == 1 else K // max(scale.shape[-1], 1)
     want = (N,) if group_size == 0 else (N, K // group_size if group_size else 0)
@@ -294,8 +316,8 @@ def linear_silu_mul(x: torch.Tensor, packed: torch.Tensor, scale: torch.Tensor,
     x2 = x.reshape(M, K).contiguous()
     N2 = packed.shape[0]
     N = N2 // 2
-    if packed.shape[1] * 4 != K:
-        raise ValueError(f"packed is [2N, {packed.shape[1]}] but K/4 = {K / 4}")
+    if packed.shape[1] != row_bytes(K):
+        raise ValueError(f"packed is [2N, {packed.shape[1]}] but ceil(K/4) = {row_bytes(K)}")
     if group_size is None:
         group_size = 0 if scale.dim() == 1 else K // max(scale.shape[-1], 1)
     want = (N2,) if group_size == 0 else (N2, K // group_size if group_size else 0)

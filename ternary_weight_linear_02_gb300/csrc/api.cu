@@ -157,10 +157,10 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
     *noop = false;
     if (x_dtype != TL_F16 && x_dtype != TL_BF16) return TL_ERR_DTYPE;
     if (out_dtype != TL_F16 && out_dtype != TL_BF16 && out_dtype != TL_F32) return TL_ERR_DTYPE;
-    if (group_size != 0 && group_size != 64 && group_size != 128 && group_size != 256)
+    if (group_size != 0 && group_size != 32 && group_size != 64 && group_size != 128 &&
+        group_size != 256)
         return TL_ERR_DTYPE;
     if (M < 0 || N < 0 || K < 0) return TL_ERR_SHAPE;
-    if (K % 4 != 0) return TL_ERR_SHAPE;
     if (group_size > 0 && K % group_size != 0) return TL_ERR_SHAPE;
     const int64_t lim = (int64_t)1 << 30;
     if (M >= lim || N >= lim || K >= lim) return TL_ERR_SHAPE;
@@ -171,11 +171,33 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
     if (out == nullptr) return TL_ERR_NULL;
     if (K > 0 && (x == nullptr || packed == nullptr)) return TL_ERR_NULL;
     if (scale == nullptr && (group_size == 0 || K > 0)) return TL_ERR_NULL;
-    if (K % 64 != 0) return TL_ERR_ALIGN;
     if (!aligned16(out) || (x && !aligned16(x)) || (packed && !aligned16(packed)) ||
         (scale && !aligned16(scale)))
         return TL_ERR_ALIGN;
     return TL_OK;
+}
+
+int gshift_of(int32_t group_size) {
+    return group_size == 32 ? 5 : group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
+}
+
+// The CUDA-core kernel for shapes the TMA-fed kernels cannot take (K % 64 != 0:
+// packed rows are not 16-byte pitched).  It does not read a zero-block map.
+tl_status run_generic(const void *x, bool bf, const uint8_t *packed, const void *scale,
+                      int32_t group_size, void *out, int32_t out_dtype, int64_t M, int64_t N,
+                      int64_t K, int64_t nh, cudaStream_t st) {
+    tl::GenArgs a{};
+    a.x = static_cast<const uint16_t *>(x);
+    a.packed = packed;
+    a.scale = static_cast<const uint16_t *>(scale);
+    a.out = out;
+    a.M = (int)M;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.gshift = gshift_of(group_size);
+    a.nh = (int)nh;
+    a.odt = out_dtype;
+    return from_cuda(tl::launch_generic(a, bf, group_size != 0, nh > 0, st, pdl_enabled()));
 }
 
 tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
@@ -186,7 +208,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     tl_status s = check_linear(x, x_dtype, packed, scale, group_size, out, out_dtype, M, N, K,
                                &noop);
     if (s != TL_OK || noop) return s;
-    if (path != TL_PATH_AUTO && path != TL_PATH_SKINNY && path != TL_PATH_TILE)
+    if (path != TL_PATH_AUTO && path != TL_PATH_SKINNY && path != TL_PATH_TILE &&
+        path != TL_PATH_GENERIC)
         return TL_ERR_DTYPE;
     if (flags & ~(uint32_t)TL_FLAG_STATIC_WEIGHTS) return TL_ERR_DTYPE;
     if (take_injected_failure()) return TL_ERR_CUDA;
@@ -197,25 +220,30 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)(M * N) * dtype_size(out_dtype), st));
 
     const bool bf = x_dtype == TL_BF16;
+    if (path == TL_PATH_GENERIC || (path == TL_PATH_AUTO && K % 64 != 0))
+        return run_generic(x, bf, packed, scale, group_size, out, out_dtype, M, N, K, 0, st);
+    if (K % 64 != 0) return TL_ERR_UNSUPPORTED;
     const bool group = group_size != 0;
-    const bool g64 = group_size == 64;
-    const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
+    // groups narrower than 128: no tcgen05 skinny kernel; 32-wide: tile kernel only
+    const bool narrow = group_size == 64 || group_size == 32;
+    const bool g32 = group_size == 32;
+    const int gshift = gshift_of(group_size);
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
     const int impl = skinny_impl();
     const bool tile_ok = tl::tile_supported(M, N, K);
     // skinny candidates: the decode kernel (M <= 16, any group size), then the
     // tcgen05 skinny kernel (M <= 32, not 64-wide groups)
     tl::GemvPlan gp{};
-    if (impl == kImplAuto && M <= tl::kGemvMaxM)
+    if (impl == kImplAuto && M <= tl::kGemvMaxM && !g32)
         gp = tl::plan_gemv(M, N, K, d->sm_count, false, group, force_sk);
     tl::SkinnyTcPlan tp{};
     tl::SkinnyPlan mp{};
     // the zero-block map is read by the decode kernel and the tile kernel only
-    if (!gp.ok && !g64 && impl != kImplMma && mask == nullptr) {
+    if (!gp.ok && !narrow && impl != kImplMma && mask == nullptr) {
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
     }
-    if (!g64 && impl == kImplMma && mask == nullptr) mp = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
+    if (!narrow && impl == kImplMma && mask == nullptr) mp = tl::plan_skinny(M, N, K, d->sm_count, force_sk);
     const bool skinny_ok = gp.ok || tp.ok || mp.ok;
     int use = path;
     if (use == TL_PATH_AUTO) {
@@ -306,10 +334,13 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     // K == 0: g = u = 0 and silu(0) * 0 = 0
     if (K == 0) return from_cuda(cudaMemsetAsync(out, 0, (size_t)(M * N) * dtype_size(out_dtype), st));
     const bool bf = x_dtype == TL_BF16;
+    if (K % 64 != 0)
+        return run_generic(x, bf, packed, scale, group_size, out, out_dtype, M, 2 * N, K, N, st);
     const bool group = group_size != 0;
-    const int gshift = group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
+    const int gshift = gshift_of(group_size);
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
-    if (M <= skinny_max_m() && M <= tl::kGemvMaxM && skinny_impl() == kImplAuto) {
+    if (M <= skinny_max_m() && M <= tl::kGemvMaxM && skinny_impl() == kImplAuto &&
+        group_size != 32) {
         tl::GemvPlan gp = tl::plan_gemv(M, 2 * N, K, d->sm_count, true, group_size != 0, force_sk);
         if (gp.ok) {
             tl::GemvArgs a{};
@@ -331,7 +362,7 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
             return from_cuda(tl::launch_gemv_silu(a, bf, group, gp, st, pdl_enabled()));
         }
     }
-    if (M <= skinny_max_m() && group_size != 64 && mask == nullptr) {
+    if (M <= skinny_max_m() && group_size != 64 && group_size != 32 && mask == nullptr) {
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, 2 * N, K, d->sm_count, force_sk, per_sm);
         if (tp.ok) {
@@ -369,7 +400,7 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
 
 tl_status check_packing(const void *t, const void *packed, int64_t N, int64_t K,
                         const int64_t *count) {
-    if (N < 0 || K < 0 || K % 4 != 0) return TL_ERR_SHAPE;
+    if (N < 0 || K < 0) return TL_ERR_SHAPE;
     // N * K must stay representable (and addressable): cap the element count at 2^48
     if (N >= ((int64_t)1 << 40) || K >= ((int64_t)1 << 40)) return TL_ERR_SHAPE;
     if (K > 0 && N > (((int64_t)1 << 48) / K)) return TL_ERR_SHAPE;
@@ -397,9 +428,9 @@ tl_status ternary_pack(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
         if (s != TL_OK) return s;
     }
     if (N * K == 0) return TL_OK;
-    return from_cuda(tl::launch_pack(t, packed, N * (K / 4),
-                                     reinterpret_cast<unsigned long long *>(invalid_count),
-                                     d->sm_count, st));
+    auto *cnt = reinterpret_cast<unsigned long long *>(invalid_count);
+    if (K % 4 != 0) return from_cuda(tl::launch_pack_rows(t, packed, N, K, cnt, d->sm_count, st));
+    return from_cuda(tl::launch_pack(t, packed, N * (K / 4), cnt, d->sm_count, st));
 }
 
 tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
@@ -416,9 +447,10 @@ tl_status ternary_unpack(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
         if (s != TL_OK) return s;
     }
     if (N * K == 0) return TL_OK;
-    return from_cuda(tl::launch_unpack(packed, t, N * (K / 4),
-                                       reinterpret_cast<unsigned long long *>(reserved_count),
-                                       d->sm_count, st));
+    auto *cnt = reinterpret_cast<unsigned long long *>(reserved_count);
+    if (K % 4 != 0)
+        return from_cuda(tl::launch_unpack_rows(packed, t, N, K, cnt, d->sm_count, st));
+    return from_cuda(tl::launch_unpack(packed, t, N * (K / 4), cnt, d->sm_count, st));
 }
 
 tl_status ternary_linear(const void *x, int32_t x_dtype, const uint8_t *packed, const void *scale,
@@ -445,13 +477,13 @@ tl_status ternary_linear_silu_mul(const void *x, int32_t x_dtype, const uint8_t 
 }
 
 int64_t ternary_block_mask_words(int64_t N, int64_t K) {
-    if (N < 0 || K < 0 || K % 4 != 0) return -1;
+    if (N < 0 || K < 0) return -1;
     return ((N + 127) / 128) * (int64_t)tl::mask_words(K);
 }
 
 tl_status ternary_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32_t *mask,
                              int64_t *zero_blocks, void *stream) {
-    if (N < 0 || K < 0 || K % 4 != 0) return TL_ERR_SHAPE;
+    if (N < 0 || K < 0) return TL_ERR_SHAPE;
     if (N >= ((int64_t)1 << 31) || K >= ((int64_t)1 << 31)) return TL_ERR_SHAPE;
     if (N * K > 0 && (packed == nullptr || mask == nullptr)) return TL_ERR_NULL;
     if ((mask && (reinterpret_cast<uintptr_t>(mask) & 3u)) ||
@@ -514,8 +546,8 @@ const char *ternary_status_string(int32_t status) {
     case TL_OK: return "TL_OK";
     case TL_ERR_NULL: return "TL_ERR_NULL: a required pointer is NULL";
     case TL_ERR_SHAPE: return "TL_ERR_SHAPE: invalid or unsupported sizes";
-    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size (0, 64, 128, 256) or path code";
-    case TL_ERR_ALIGN: return "TL_ERR_ALIGN: pointer not 16-byte aligned or K % 64 != 0";
+    case TL_ERR_DTYPE: return "TL_ERR_DTYPE: unknown dtype, group size (0, 32, 64, 128, 256) or path code";
+    case TL_ERR_ALIGN: return "TL_ERR_ALIGN: pointer not 16-byte aligned";
     case TL_ERR_VALUE: return "TL_ERR_VALUE: invalid or reserved values present";
     case TL_ERR_CUDA: return "TL_ERR_CUDA: a CUDA call or kernel launch failed";
     case TL_ERR_TIMEOUT: return "TL_ERR_TIMEOUT: a bounded device-side wait gave up";

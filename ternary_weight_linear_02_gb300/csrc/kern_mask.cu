@@ -9,6 +9,9 @@
 // non-zero exactly when b0 != b1, so a byte holds a non-zero weight when
 // (byte ^ (byte >> 1)) & 0x55 != 0.
 //
+// Rows are ceil(K/4) bytes; when K % 4 != 0 the last byte's fields past K are
+// padding (the Qwen2.5-7B write-up §2.3) and are masked off before the test.
+//
 // One thread per block: a warp covers 32 consecutive k-blocks of one row block
 // (512 contiguous bytes of each row, so its loads are coalesced) and writes
 // one 32-bit word of the map with a ballot.  HBM-bound: the packed matrix is
@@ -25,7 +28,9 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const uint8_t *packed, 
     const int64_t rb = blockIdx.x;
     const int w = blockIdx.y * 8 + (threadIdx.x >> 5);  // map word of this warp
     if (w >= words) return;
-    const int64_t Kq = K >> 2;                          // bytes per packed row
+    const int64_t Kq = (K + 3) >> 2;                    // bytes per packed row
+    // weight fields of the row's last byte (padding fields cleared)
+    const uint32_t last = (K & 3) ? (1u << (2 * (K & 3))) - 1u : 0xFFu;
     const int64_t KB = (K + 63) >> 6;
     const int64_t kb = (int64_t)w * 32 + lane;
     const bool valid = kb < KB;
@@ -33,7 +38,7 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const uint8_t *packed, 
     if (valid) {
         const int64_t b0 = kb * 16, b1 = b0 + 16 < Kq ? b0 + 16 : Kq;
         const int64_t r0 = rb * 128, r1 = r0 + 128 < N ? r0 + 128 : N;
-        if ((Kq & 15) == 0) {
+        if ((K & 63) == 0) {  // whole 16-byte segments, no padding
             for (int64_t n = r0; n < r1; ++n) {
                 const uint4 v = ldg_nc_v4(packed + n * Kq + b0);
                 nz |= ((v.x ^ (v.x >> 1)) | (v.y ^ (v.y >> 1)) | (v.z ^ (v.z >> 1)) |
@@ -42,7 +47,7 @@ __global__ void __launch_bounds__(256) block_mask_kernel(const uint8_t *packed, 
         } else {
             for (int64_t n = r0; n < r1; ++n)
                 for (int64_t b = b0; b < b1; ++b) {
-                    const uint32_t v = packed[n * Kq + b];
+                    const uint32_t v = packed[n * Kq + b] & (b == Kq - 1 ? last : 0xFFu);
                     nz |= (v ^ (v >> 1)) & 0x55u;
                 }
         }

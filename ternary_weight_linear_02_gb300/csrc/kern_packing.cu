@@ -4,11 +4,18 @@
 // (trdm.cn/news/729035) §3.1; the Qwen2.5-7B ternary-in-vLLM write-up
 // (m.nxbn.cn/news/169761) §2.2 (reserved code counted as a format check).
 //
-// Both kernels are pure streaming: packed byte i holds the four weights
-// 4i..4i+3 of the flattened [N,K] matrix (rows are dense, so the row split does
-// not matter).  One thread handles 16 packed bytes (one 16-byte load) and the
-// 64 int8 weights they expand to; a scalar loop covers the ragged tail.  The
-// grid is a multiple of the SM count, grid-striding over the array.
+// K % 4 == 0: both kernels are pure streaming: packed byte i holds the four
+// weights 4i..4i+3 of the flattened [N,K] matrix (rows are dense, so the row
+// split does not matter).  One thread handles 16 packed bytes (one 16-byte
+// load) and the 64 int8 weights they expand to; a scalar loop covers the
+// ragged tail.  The grid is a multiple of the SM count, grid-striding over the
+// array.
+//
+// K % 4 != 0: a row takes ceil(K/4) bytes and the last byte's fields past K are
+// padding (the Qwen2.5-7B write-up §2.3: an export pads rows to whole bytes and
+// the padding is cut off after unpacking).  The *_rows kernels take one packed
+// byte per thread; pack writes padding fields as 00, unpack neither writes nor
+// counts them.
 #include "common.cuh"
 
 namespace tl {
@@ -110,6 +117,48 @@ __global__ void __launch_bounds__(256) pack_kernel(const int8_t *__restrict__ t,
     }
 }
 
+__global__ void __launch_bounds__(256) unpack_rows_kernel(const uint8_t *__restrict__ packed,
+                                                          int8_t *__restrict__ t, int64_t N,
+                                                          int64_t K, unsigned long long *reserved) {
+    const int64_t Kq = (K + 3) >> 2, nbytes = N * Kq;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    uint32_t cnt = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes; i += stride) {
+        const int64_t n = i / Kq, b = i - n * Kq;
+        const int nf = (int)min((int64_t)4, K - 4 * b);  // fields of this byte that are weights
+        uint32_t byte = packed[i];
+        if (nf < 4) byte &= (1u << (2 * nf)) - 1u;       // drop the padding fields
+        const uint32_t o = unpack_byte(byte);
+        int8_t *dst = t + n * K + 4 * b;
+        for (int j = 0; j < nf; ++j) dst[j] = (int8_t)((o >> (8 * j)) & 0xFFu);
+        if (reserved) cnt += reserved_in_byte(byte);
+    }
+    if (reserved) {
+        for (int off = 16; off; off >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        if ((threadIdx.x & 31) == 0 && cnt) atomicAdd(reserved, (unsigned long long)cnt);
+    }
+}
+
+__global__ void __launch_bounds__(256) pack_rows_kernel(const int8_t *__restrict__ t,
+                                                        uint8_t *__restrict__ packed, int64_t N,
+                                                        int64_t K, unsigned long long *invalid_out) {
+    const int64_t Kq = (K + 3) >> 2, nbytes = N * Kq;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    uint32_t bad = 0;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nbytes; i += stride) {
+        const int64_t n = i / Kq, b = i - n * Kq;
+        const int nf = (int)min((int64_t)4, K - 4 * b);
+        const int8_t *src = t + n * K + 4 * b;
+        uint32_t w = 0;  // padding lanes stay 0: written 00, never counted invalid
+        for (int j = 0; j < nf; ++j) w |= (uint32_t)(uint8_t)src[j] << (8 * j);
+        packed[i] = (uint8_t)pack_word(w, bad);
+    }
+    if (invalid_out) {
+        for (int off = 16; off; off >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, off);
+        if ((threadIdx.x & 31) == 0 && bad) atomicAdd(invalid_out, (unsigned long long)bad);
+    }
+}
+
 static int grid_for(int64_t work_items, int sm_count) {
     int64_t blocks = (work_items + 255) / 256;
     int64_t cap = (int64_t)sm_count * 8;
@@ -129,6 +178,20 @@ cudaError_t launch_pack(const int8_t *t, uint8_t *packed, int64_t nbytes,
                         unsigned long long *invalid, int sm_count, cudaStream_t st) {
     int64_t items = nbytes / 16 > 0 ? nbytes / 16 : nbytes;
     pack_kernel<<<grid_for(items, sm_count), 256, 0, st>>>(t, packed, nbytes, invalid);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_rows(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
+                               unsigned long long *reserved, int sm_count, cudaStream_t st) {
+    unpack_rows_kernel<<<grid_for(N * ((K + 3) / 4), sm_count), 256, 0, st>>>(packed, t, N, K,
+                                                                             reserved);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_rows(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
+                             unsigned long long *invalid, int sm_count, cudaStream_t st) {
+    pack_rows_kernel<<<grid_for(N * ((K + 3) / 4), sm_count), 256, 0, st>>>(t, packed, N, K,
+                                                                           invalid);
     return cudaGetLastError();
 }
 

@@ -13,6 +13,11 @@ cudaError_t launch_unpack(const uint8_t *packed, int8_t *t, int64_t nbytes,
                           unsigned long long *reserved, int sm_count, cudaStream_t st);
 cudaError_t launch_pack(const int8_t *t, uint8_t *packed, int64_t nbytes,
                         unsigned long long *invalid, int sm_count, cudaStream_t st);
+// K % 4 != 0: rows of ceil(K/4) bytes, padding fields 00 on pack, skipped on unpack
+cudaError_t launch_unpack_rows(const uint8_t *packed, int8_t *t, int64_t N, int64_t K,
+                               unsigned long long *reserved, int sm_count, cudaStream_t st);
+cudaError_t launch_pack_rows(const int8_t *t, uint8_t *packed, int64_t N, int64_t K,
+                             unsigned long long *invalid, int sm_count, cudaStream_t st);
 
 // ------------------------------------------------------------ zero-block map
 // bit kb%32 of word [rb][kb/32]: rows [128 rb, +128) x k [64 kb, +64) hold a non-zero weight
@@ -156,11 +161,25 @@ struct TileArgs {
     int mask_words;          // map words per 128-row block
 };
 
-bool tile_supported(int64_t M, int64_t N, int64_t K);
+bool tile_supported(int64_t M, int64_t N, int64_t K);  // K % 64 == 0
 cudaError_t launch_tile(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
                         cudaStream_t st, bool pdl);
 // SiLU-gated gate/up product on the tile kernel: a.N = 2 * a.nh stacked rows, out [M, nh]
 cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype,
                              cudaStream_t st, bool pdl);
+
+// ------------------------------------------------------------ generic path (K % 64 != 0)
+struct GenArgs {
+    const uint16_t *x;       // [M,K] fp16 or bf16 bits
+    const uint8_t *packed;   // [N,K/4]
+    const uint16_t *scale;   // fp16 [N] or [N,K/G]
+    void *out;               // [M,N] (gated: [M,nh])
+    int M, N, K;             // packed rows of ceil(K/4) bytes; N = every stacked row (gated: 2 * nh)
+    int gshift;              // log2 of the group size G (5, 6, 7 or 8) in group mode
+    int nh;                  // gated call: gate rows [0, nh), up rows [nh, 2 nh)
+    int odt;                 // output dtype: 0 fp16, 1 bf16, 2 fp32
+};
+cudaError_t launch_generic(const GenArgs &a, bool bf, bool group, bool silu, cudaStream_t st,
+                           bool pdl);
 
 }  // namespace tl

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t Kq = a.K >> 2;
         const uint8_t *prow = a.packed + (int64_t)(rowok ? n : 0) * Kq;
         const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
-        const int ngk = a.K >> a.gshift;  // scale groups per row (G = 64, 128 or 256)
+        const int ngk = a.K >> a.gshift;  // scale groups per row (G = 32, 64, 128 or 256)
         const uint16_t *srow = a.scale + (SMODE == kChannel ? 0 : (int64_t)(rowok ? n : 0) * ngk);
 
         // live chunks c (current), c1 and c2 (codes loaded one and two chunks ahead)
@@ -243,31 +243,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             decode_word_adjacent(codes.w, r + 24);
             uint32_t rl[32];
             if constexpr (SMODE != kChannel) {
-                const uint16_t sbits = rowok ? srow[(c * kKC) >> a.gshift] : (uint16_t)0;
-                const float sf = h2f(sbits);
-                if constexpr (SMODE == kFold) {
-                    // fp16: (+-2) * (s/2) = +-s exactly
-                    const __half2 h2 = __half2half2(__float2half_rn(0.5f * sf));
+                // registers 0-15 hold k 0-31 of the chunk, 16-31 hold k 32-63: with
+                // 32-wide groups the two halves have their own scales (the same one
+                // for wider groups); an adjacent pair never straddles a group
+                const uint16_t sb0 = rowok ? srow[(c * kKC) >> a.gshift] : (uint16_t)0;
+                const uint16_t sb1 = rowok ? srow[(c * kKC + 32) >> a.gshift] : (uint16_t)0;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        __half2 v = *reinterpret_cast<__half2 *>(&r[i]);
-                        v = __hmul2(v, h2);
-                        r[i] = *reinterpret_cast<uint32_t *>(&v);
-                    }
-                } else {
-                    // bf16: s = s_hi + s_lo, both exact in bf16
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(sf);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(sf - __bfloat162float(hi));
-                    const __nv_bfloat162 h2 =
-                        __bfloat162bfloat162(__float2bfloat16_rn(0.5f * __bfloat162float(hi)));
-                    const __nv_bfloat162 l2 =
-                        __bfloat162bfloat162(__float2bfloat16_rn(0.5f * __bfloat162float(lo)));
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float sf = h2f(hf ? sb1 : sb0);
+                    if constexpr (SMODE == kFold) {
+                        // fp16: (+-2) * (s/2) = +-s exactly
+                        const __half2 h2 = __half2half2(__float2half_rn(0.5f * sf));
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r[i]);
-                        __nv_bfloat162 vh = __hmul2(v, h2), vl = __hmul2(v, l2);
-                        r[i] = *reinterpret_cast<uint32_t *>(&vh);
-                        rl[i] = *reinterpret_cast<uint32_t *>(&vl);
+                        for (int i = 16 * hf; i < 16 * hf + 16; ++i) {
+                            __half2 v = *reinterpret_cast<__half2 *>(&r[i]);
+                            v = __hmul2(v, h2);
+                            r[i] = *reinterpret_cast<uint32_t *>(&v);
+                        }
+                    } else {
+                        // bf16: s = s_hi + s_lo, both exact in bf16
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(sf);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(sf - __bfloat162float(hi));
+                        const __nv_bfloat162 h2 =
+                            __bfloat162bfloat162(__float2bfloat16_rn(0.5f * __bfloat162float(hi)));
+                        const __nv_bfloat162 l2 =
+                            __bfloat162bfloat162(__float2bfloat16_rn(0.5f * __bfloat162float(lo)));
+#pragma unroll
+                        for (int i = 16 * hf; i < 16 * hf + 16; ++i) {
+                            __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162 *>(&r[i]);
+                            __nv_bfloat162 vh = __hmul2(v, h2), vl = __hmul2(v, l2);
+                            r[i] = *reinterpret_cast<uint32_t *>(&vh);
+                            rl[i] = *reinterpret_cast<uint32_t *>(&vl);
+                        }
                     }
                 }
             }

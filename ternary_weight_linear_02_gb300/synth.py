@@ -42,24 +42,25 @@ def _gen(seed: int, device) -> torch.Generator:
 
 def packed_codes(N: int, K: int, seed: int, device="cpu", p_reserved: float = 0.0,
                  chunk_rows: int | None = None) -> torch.Tensor:
-    """Random packed weights [N, K/4] uint8 with the code distribution above."""
-    if K % 4:
-        raise ValueError("K must be a multiple of 4")
+    """Random packed weights [N, ceil(K/4)] uint8 with the code distribution above.
+    When K % 4 != 0 the last byte's padding fields are drawn like the rest (any
+    code, 11 included), so a reader that took them for weights would be seen."""
     dev = torch.device(device)
-    out = torch.empty((N, K // 4), dtype=torch.uint8, device=dev)
+    Kq = (K + 3) // 4
+    out = torch.empty((N, Kq), dtype=torch.uint8, device=dev)
     g = _gen(seed, dev)
     if chunk_rows is None:
         chunk_rows = max(1, (1 << 26) // max(K, 1))
     lo, hi = CODE_P[0], CODE_P[0] + CODE_P[1]
     for r0 in range(0, N, chunk_rows):
         r1 = min(N, r0 + chunk_rows)
-        u = torch.rand((r1 - r0, K // 4, 4), generator=g, device=dev)
+        u = torch.rand((r1 - r0, Kq, 4), generator=g, device=dev)
         codes = torch.zeros_like(u, dtype=torch.uint8)
         codes[(u >= lo) & (u < hi)] = 1
         codes[u >= hi] = 2
         if p_reserved > 0.0:
-            hit = torch.rand((r1 - r0, K // 4), generator=g, device=dev) < p_reserved
-            field = torch.randint(0, 4, (r1 - r0, K // 4), generator=g, device=dev)
+            hit = torch.rand((r1 - r0, Kq), generator=g, device=dev) < p_reserved
+            field = torch.randint(0, 4, (r1 - r0, Kq), generator=g, device=dev)
             sel = torch.nn.functional.one_hot(field, 4).to(torch.bool) & hit.unsqueeze(-1)
             codes[sel] = 3
         byte = (codes[..., 0] | (codes[..., 1] << 2) | (codes[..., 2] << 4)

@@ -64,7 +64,7 @@ def test_status_strings(lib):
         assert lib.ternary_status_string(s)
     assert b"unknown" in lib.ternary_status_string(99)
     # the accepted group sizes are named
-    assert b"(0, 64, 128, 256)" in lib.ternary_status_string(TL_ERR_DTYPE)
+    assert b"(0, 32, 64, 128, 256)" in lib.ternary_status_string(TL_ERR_DTYPE)
     assert lib.ternary_version() >= 100
 
 
@@ -79,18 +79,19 @@ def test_linear_argument_errors(lib):
     assert lin(lib, xdt=2) == TL_ERR_DTYPE          # fp32 x not supported
     assert lin(lib, xdt=-1) == TL_ERR_DTYPE
     assert lin(lib, odt=5) == TL_ERR_DTYPE
-    assert lin(lib, gs=32) == TL_ERR_DTYPE          # group sizes: 0, 64, 128, 256
+    assert lin(lib, gs=16) == TL_ERR_DTYPE          # group sizes: 0, 32, 64, 128, 256
+    assert lin(lib, gs=48) == TL_ERR_DTYPE
     assert lin(lib, gs=512) == TL_ERR_DTYPE
     assert lin(lib, path=7) == TL_ERR_DTYPE
     assert lin(lib, flags=2) == TL_ERR_DTYPE
     assert lin(lib, M=-1) == TL_ERR_SHAPE
     assert lin(lib, N=-2) == TL_ERR_SHAPE
-    assert lin(lib, K=130) == TL_ERR_SHAPE           # K % 4
+    assert lin(lib, K=-3) == TL_ERR_SHAPE
     assert lin(lib, gs=128, K=192) == TL_ERR_SHAPE   # K % 128 in group mode
     assert lin(lib, gs=64, K=96) == TL_ERR_SHAPE     # K % 64 in 64-wide group mode
     assert lin(lib, gs=256, K=384) == TL_ERR_SHAPE   # K % 256 in 256-wide group mode
+    assert lin(lib, gs=32, K=48) == TL_ERR_SHAPE     # K % 32 in 32-wide group mode
     assert lin(lib, M=1 << 31) == TL_ERR_SHAPE
-    assert lin(lib, K=96) == TL_ERR_ALIGN             # K % 64
     assert lin(lib, out=0) == TL_ERR_NULL
     assert lin(lib, x=0) == TL_ERR_NULL
     assert lin(lib, packed=0) == TL_ERR_NULL
@@ -119,12 +120,12 @@ def silu(lib, x=A, xdt=1, packed=B, scale=C, gs=0, out=D, odt=2, M=4, N=8, K=128
 
 def test_silu_mul_argument_errors(lib):
     # checked on the host before any device work
-    assert silu(lib, gs=32) == TL_ERR_DTYPE
+    assert silu(lib, gs=16) == TL_ERR_DTYPE
+    assert silu(lib, gs=32, K=48) == TL_ERR_SHAPE
     assert silu(lib, flags=4) == TL_ERR_DTYPE
     assert silu(lib, N=-1) == TL_ERR_SHAPE
-    assert silu(lib, K=130) == TL_ERR_SHAPE
+    assert silu(lib, gs=64, K=130) == TL_ERR_SHAPE   # K % 64 in 64-wide group mode
     assert silu(lib, gs=256, K=384) == TL_ERR_SHAPE
-    assert silu(lib, K=96) == TL_ERR_ALIGN
     assert silu(lib, out=0) == TL_ERR_NULL
     assert silu(lib, packed=B + 1) == TL_ERR_ALIGN
     assert silu(lib, M=0, x=0, out=0) == TL_OK         # empty: no-op
@@ -133,9 +134,12 @@ def test_silu_mul_argument_errors(lib):
 
 def test_packing_argument_errors(lib):
     p = ctypes.c_void_p
-    assert lib.ternary_pack(p(A), p(B), 4, 6, None, None) == TL_ERR_SHAPE
+    assert lib.ternary_pack(p(A), p(B), 4, -6, None, None) == TL_ERR_SHAPE
     assert lib.ternary_pack(p(A), p(B), -1, 8, None, None) == TL_ERR_SHAPE
-    assert lib.ternary_unpack(p(B), p(A), 4, 10, None, None) == TL_ERR_SHAPE
+    assert lib.ternary_unpack(p(B), p(A), 4, -10, None, None) == TL_ERR_SHAPE
+    # K % 4 != 0 is a padded row, not an error: the checks pass up to the device query
+    assert lib.ternary_pack(p(A), p(B), 4, 6, None, None) != TL_ERR_SHAPE
+    assert lib.ternary_unpack(p(B), p(A), 4, 10, None, None) != TL_ERR_SHAPE
     assert lib.ternary_pack(None, p(B), 4, 8, None, None) == TL_ERR_NULL
     assert lib.ternary_unpack(p(B), None, 4, 8, None, None) == TL_ERR_NULL
     assert lib.ternary_pack(p(A + 1), p(B), 4, 8, None, None) == TL_ERR_ALIGN
@@ -186,8 +190,9 @@ def test_block_mask_host_checks(lib):
     p = ctypes.c_void_p
     assert lib.ternary_block_mask_words(300, 4160) == 3 * 3
     assert lib.ternary_block_mask_words(0, 64) == 0
-    assert lib.ternary_block_mask_words(4, 6) == -1
-    assert lib.ternary_block_mask(p(B), 4, 6, p(A), None, None) == TL_ERR_SHAPE
+    assert lib.ternary_block_mask_words(4, 6) == 1     # K % 4 != 0: padded rows
+    assert lib.ternary_block_mask_words(4, -6) == -1
+    assert lib.ternary_block_mask(p(B), 4, -6, p(A), None, None) == TL_ERR_SHAPE
     assert lib.ternary_block_mask(None, 4, 8, p(A), None, None) == TL_ERR_NULL
     assert lib.ternary_block_mask(p(B), 4, 8, p(A + 2), None, None) == TL_ERR_ALIGN
     assert lib.ternary_block_mask(p(B), 4, 8, p(A), p(C + 4), None) == TL_ERR_ALIGN
@@ -200,7 +205,7 @@ def test_masked_linear_host_checks(lib):
                                      None) == TL_ERR_NULL
     assert lib.ternary_linear_masked(v(A), 0, v(B), v(C), 0, v(A + 2), v(D), 2, 4, 8, 128, 0,
                                      None) == TL_ERR_ALIGN
-    assert lib.ternary_linear_masked(v(A), 0, v(B), v(C), 0, v(A), v(D), 2, 4, 8, 130, 0,
+    assert lib.ternary_linear_masked(v(A), 0, v(B), v(C), 128, v(A), v(D), 2, 4, 8, 130, 0,
                                      None) == TL_ERR_SHAPE
-    assert lib.ternary_linear_silu_mul_masked(v(A), 0, v(B), v(C), 32, v(A), v(D), 2, 4, 8, 128,
+    assert lib.ternary_linear_silu_mul_masked(v(A), 0, v(B), v(C), 16, v(A), v(D), 2, 4, 8, 128,
                                               0, None) == TL_ERR_DTYPE

@@ -53,9 +53,43 @@ def test_split_k_rejects_misaligned_cuts():
     _, p, s = synth.layer(1, 8, 512, torch.float16, 128, 0.005, 0.05, ("shard-bad",), "cpu")
     with pytest.raises(ValueError):
         shard.split_k(p, s, [192, 320])          # 192 splits a 128-wide group
-    _, p0, s0 = synth.layer(1, 8, 512, torch.float16, 0, 0.005, 0.05, ("shard-bad0",), "cpu")
-    shard.split_k(p0, s0, [192, 320])            # per channel: multiples of 64 are fine
+    _, p32, s32 = synth.layer(1, 8, 512, torch.float16, 32, 0.005, 0.05, ("shard-32",), "cpu")
+    shard.split_k(p32, s32, [96, 416])           # whole 32-wide groups
     with pytest.raises(ValueError):
-        shard.split_k(p0, s0, [96, 416])
+        shard.split_k(p32, s32, [100, 412])
+    _, p0, s0 = synth.layer(1, 8, 512, torch.float16, 0, 0.005, 0.05, ("shard-bad0",), "cpu")
+    shard.split_k(p0, s0, [192, 320])            # per channel: any byte boundary slices
+    shard.split_k(p0, s0, [96, 416])
+    with pytest.raises(ValueError, match="device"):
+        shard.split_k(p0, s0, [97, 415])         # off a byte boundary: repacked on the device only
+    with pytest.raises(ValueError):
+        shard.split_k(p0, s0, [0, 512])
     with pytest.raises(ValueError):
         shard.split_n(p0, s0, [4, 3])
+
+
+@pytest.mark.parametrize("gs,sizes", [(0, [96, 4, 412]), (32, [160, 352]), (64, [64, 448])])
+def test_split_k_byte_aligned_cuts_sum_to_full(gs, sizes):
+    """Byte-aligned cuts off the 64-k grid are plain slices; the shards' oracle
+    results add up to the whole layer's."""
+    M, N, K = 3, 40, 512
+    x, p, s = synth.layer(M, N, K, torch.bfloat16, gs, 0.005, 0.05, ("shard-byte", gs), "cpu", 0.01)
+    full = oracle_ref(x, p, s, gs)
+    total = np.zeros_like(full)
+    for (pi, si, k0), k in zip(shard.split_k(p, s, sizes), sizes):
+        assert pi.shape == (N, (k + 3) // 4)
+        total += oracle_ref(x[:, k0:k0 + k].contiguous(), pi, si, gs)
+    np.testing.assert_allclose(total, full, rtol=1e-12, atol=1e-12)
+
+
+def test_split_k_last_shard_keeps_padding():
+    """K % 4 != 0: a last shard that starts on a byte boundary is a plain slice
+    whose last byte carries the layer's padding fields."""
+    M, N, K = 2, 16, 103
+    x, p, s = synth.layer(M, N, K, torch.float16, 0, 0.005, 0.05, ("shard-pad",), "cpu", 0.01)
+    parts = shard.split_k(p, s, [64, 39], K=K)
+    assert parts[1][0].shape == (N, 10)
+    full = oracle_ref(x, p, s, 0)
+    total = sum(oracle_ref(x[:, k0:k0 + k].contiguous(), pi, si, 0)
+                for (pi, si, k0), k in zip(parts, [64, 39]))
+    np.testing.assert_allclose(total, full, rtol=1e-12, atol=1e-12)
