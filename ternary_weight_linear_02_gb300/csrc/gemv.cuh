@@ -139,29 +139,6 @@ __device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t 
     }
 }
 
-__device__ __forceinline__ uint32_t cl_map(uint32_t saddr, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void cl_st_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void cl_st_u32(uint32_t addr, uint32_t v) {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ void cl_arrive_relaxed() {
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cl_wait() {
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cl_arrive_release() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cl_wait_acquire() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ float silu(float v) { return v / (1.f + expf(-v)); }
 
@@ -220,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int n0 = blockIdx.x * RB, j0 = blockIdx.x * PH;
     const long long lim = a.wait_limit;
 
-    if (sk > 1) cl_arrive_relaxed();  // cluster phase 1: this CTA has started
+    if (sk > 1) cluster_arrive_relaxed();  // cluster phase 1: this CTA has started
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.ws; ++i) {
             mbar_init(&full[i], 1);
@@ -546,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 
     // ------------------------------------------------ split K over the cluster
     // owner q holds rows [q*RB/sk, (q+1)*RB/sk) (gated: pairs [q*PH/sk, (q+1)*PH/sk))
-    cl_wait();  // phase 1: every peer runs
+    cluster_wait();  // phase 1: every peer runs
     constexpr int span = SILU ? PH : RB;
     const int SL = (span + sk - 1) / sk;
     auto owner = [&](int p) {

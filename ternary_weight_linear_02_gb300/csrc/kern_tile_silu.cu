@@ -7,7 +7,7 @@ namespace tl {
 
 cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype,
                              cudaStream_t st, bool pdl) {
-    return launch_tile_any<true>(a, bf, group, out_dtype, st, pdl);
+    return launch_tile_any<true>(a, bf, group, out_dtype, 0, st, pdl);  // no split K
 }
 
 }  // namespace tl

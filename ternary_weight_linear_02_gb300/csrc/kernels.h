@@ -159,6 +159,8 @@ struct TileArgs {
     int *status;             // device status word (bounded-wait failures)
     const uint32_t *mask;    // zero-block map of packed (nullptr: every block is read)
     int mask_words;          // map words per 128-row block
+    int sk;                  // K split = cluster size along grid z (set by the launcher)
+    int cpc;                 // 64-k chunks per CTA of the split (set by the launcher)
 };
 
 bool tile_supported(int64_t M, int64_t N, int64_t K);  // K % 64 == 0

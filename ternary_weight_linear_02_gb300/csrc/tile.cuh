@@ -32,6 +32,14 @@
 //   per group, fp16 x  -> A holds t*s[n,g] exactly (s is fp16)
 //   per group, bf16 x  -> s = s_hi + s_lo with both parts exact in bf16; two
 //                         MMAs per k step (A_hi and A_lo) into the same D.
+//  * Split K (a.sk > 1, plain output only): a cluster of sk CTAs along grid z
+//    shares one output tile; CTA r multiplies chunks [r cpc, (r + 1) cpc) into its
+//    own D.  The tile's BN token columns are dealt out in sk slices; every CTA
+//    sends slice q of its D to CTA q's shared memory (st.shared::cluster into
+//    the x ring, idle once the cluster has passed a barrier that follows every
+//    CTA's last MMA), and CTA q adds the sk partials of its slice in rank order
+//    -- the sum is the same on every run -- then scales and stores.  Fills the
+//    GPU when ceil(N/128) * ceil(M/BN) tiles alone would leave SMs idle.
 //  * SiLU-gated mode (SILU = true, a stacked gate/up layer): the CTA's 128 rows
 //    are 64 gate rows and the matching 64 up rows; in the epilogue the up lanes
 //    pass their scaled values through shared memory (the x ring, idle once D is
@@ -41,6 +49,11 @@
 #pragma once
 
 #include <cuda.h>
+#include <stdlib.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "kernels.h"
 #include "tc.cuh"
@@ -70,8 +83,19 @@ struct TileCfg {
     // shared memory: [x stages][barriers][tmem slot, abort flag] + 1 KB alignment slack
     static constexpr int BAR_OFF = kNS * XSTAGE;
     static constexpr int NBARS = 2 * kNS + 2 * NA + 1;
-    // [tmem slot, abort flag, four epilogue flags] after the barriers
-    static constexpr int SMEM = BAR_OFF + NBARS * 8 + 32 + 1024;
+    // [tmem slot, abort flag, four epilogue flags, -, -, eight split-K rank flags]
+    // after the barriers
+    static constexpr int SMEM = BAR_OFF + NBARS * 8 + 64 + 1024;
+    // Shared memory requested per CTA: at least enough that an SM holds no more CTAs
+    // than its 512 tensor-memory columns serve.  A CTA resident beyond that would wait
+    // in tcgen05.alloc; with split-K clusters its peers would wait on it at the
+    // cluster barrier while holding the columns it needs.
+    static constexpr int TMEM_CPS = (int)(512 / TMEM_COLS);
+    static constexpr int SMEM_FLOOR = TMEM_CPS >= 2 ? 80 * 1024 : 116 * 1024;
+    static constexpr int SMEM_REQ = SMEM > SMEM_FLOOR ? SMEM : SMEM_FLOOR;
+    static_assert(TMEM_CPS >= 1 && TMEM_CPS <= 2, "tensor memory budget");
+    static_assert((TMEM_CPS + 1) * (SMEM_REQ + 1024) > 228 * 1024, "residency <= tensor memory");
+    static_assert(TMEM_CPS * (SMEM_REQ + 1024) <= 228 * 1024, "shared memory");
 };
 
 // Adjacent-pair decode of one 32-bit word of 16 codes (k = 0..15 of the word)
@@ -116,6 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int j0 = blockIdx.x * 64;
     const int n0 = SILU ? j0 : blockIdx.x * 128, m0 = blockIdx.y * BN;
     const int nchunks = a.K / kKC;
+    // split K: this CTA's chunks [cb, ce) (the whole K when a.sk == 1)
+    const int krank = a.sk > 1 ? (int)cluster_ctarank() : 0;
+    const int cb = min(nchunks, krank * a.cpc), ce = a.sk > 1 ? min(nchunks, cb + a.cpc) : nchunks;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNS; ++i) {
@@ -145,6 +172,67 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a.status) atomicExch(a.status, kStatusTimeout);
     };
 
+    // Split K: the producer and MMA warps only join the cluster's two phases.
+    auto split_phases_idle = [&]() {
+        __syncwarp();
+        cl_arrive_release();  // phase 1: this CTA's work is issued and its D final
+        cl_wait_acquire();
+        cl_arrive_release();  // phase 2: partials exchanged
+        cl_wait_acquire();
+    };
+    // Split K, decoder / epilogue warps: exchange the partial D slices through the
+    // x rings, then add the slice this CTA owns in rank order, scale and store.
+    auto split_epilogue = [&](bool ready, bool ok, int lc, int row, int n, bool rowok) {
+        volatile int *wready = reinterpret_cast<volatile int *>(tmem_slot + 2);   // per epilogue warp
+        volatile int *rank_ok = reinterpret_cast<volatile int *>(tmem_slot + 8);  // per cluster rank
+        if (lane == 0) wready[warp] = ready ? 1 : 0;
+        if (!ready && ok) give_up();
+        __syncwarp();
+        cl_arrive_release();  // phase 1: every CTA's D is final (or given up), its x ring idle
+        cl_wait_acquire();
+        const bool cta_ok = !*abort_flag && wready[0] && wready[1] && wready[2] && wready[3];
+        const int sk = a.sk, slice = BN / sk, lsl = 31 - __clz(slice);
+        // receive buffer [source rank][slice column][128 rows] fp32 = 512 * BN bytes,
+        // the size of the x ring; lanes write consecutive rows (no bank conflicts)
+        const float *recv = reinterpret_cast<const float *>(smem);
+        const uint32_t recv_u32 = smem_u32(smem);
+        if (cta_ok) {
+            tc::fence_after_sync();
+#pragma unroll 1
+            for (int j = 0; j < BN / 32; ++j) {
+                uint32_t d[32];
+                tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
+                tc::wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int q = j * 32 + i;  // token column of the tile
+                    const uint32_t off =
+                        ((((uint32_t)krank << lsl) + (uint32_t)(q & (slice - 1))) * 128u + (uint32_t)row) * 4u;
+                    // lc == 0: no live chunk in this CTA's range, D was never written
+                    cl_st_f32(cl_map(recv_u32 + off, (uint32_t)(q >> lsl)), lc == 0 ? 0.f : __uint_as_float(d[i]));
+                }
+            }
+        }
+        if (threadIdx.x == 0)
+            for (int r = 0; r < sk; ++r)
+                cl_st_u32(cl_map(smem_u32((const void *)(rank_ok + krank)), (uint32_t)r), cta_ok ? 1u : 0u);
+        __syncwarp();
+        cl_arrive_release();  // phase 2: every slice's partials and every rank's flag in place
+        cl_wait_acquire();
+        bool all_ok = true;
+        for (int r = 0; r < sk; ++r) all_ok = all_ok && rank_ok[r] != 0;
+        if (!all_ok || !rowok) return;
+        // channel mode: A held 2*t, so D = 2*sum(t x); group modes: A held t*s
+        float sc = 1.f;
+        if constexpr (SMODE == kChannel) sc = 0.5f * h2f(a.scale[n]);
+        const int mb = m0 + krank * slice;
+        for (int c = 0; c < slice && mb + c < a.M; ++c) {
+            float v = 0.f;
+            for (int r = 0; r < sk; ++r) v += recv[((r << lsl) + c) * 128 + row];
+            OutStore<OUT>::st(a.out, (int64_t)(mb + c) * a.N + n, v * sc);
+        }
+    };
+
     // Zero-block map (a.mask, optional; bit kb of word [rb][kb / 32] set when rows
     // [128 rb, +128) x k [64 kb, +64) hold a non-zero weight): a 64-k chunk whose
     // blocks are zero for this CTA's rows is neither loaded nor multiplied.  All
@@ -164,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return rows_live(n0, min(n0 + 128, a.N), c);
     };
     auto next_live = [&](int c) {
-        while (c < nchunks && !chunk_live(c)) ++c;
+        while (c < ce && !chunk_live(c)) ++c;
         return c;
     };
 
@@ -173,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tc::prefetch_tmap(&tmx);
             int lc = 0;  // live chunks issued
-            for (int c = next_live(0); c < nchunks && !*abort_flag; c = next_live(c + 1), ++lc) {
+            for (int c = next_live(cb); c < ce && !*abort_flag; c = next_live(c + 1), ++lc) {
                 const int s = lc % kNS;
                 if (lc >= kNS && !mbar_wait_bounded(&xempty[s], ((lc / kNS) - 1) & 1)) {
                     give_up();
@@ -183,12 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::tma_load_2d(smem + (size_t)s * C::XSTAGE, &tmx, c * kKC, m0, &xfull[s]);
             }
         }
+        if (a.sk > 1) split_phases_idle();
     } else if (warp == 5) {
         // ---------------- MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16(BN, BF);
             int lc = 0;  // live chunks multiplied
-            for (int c = next_live(0); c < nchunks; c = next_live(c + 1), ++lc) {
+            for (int c = next_live(cb); c < ce; c = next_live(c + 1), ++lc) {
                 const int s = lc % C::NA, xs = lc % kNS;
                 if (*abort_flag || !mbar_wait_bounded(&afull[s], (lc / C::NA) & 1) ||
                     !mbar_wait_bounded(&xfull[xs], (lc / kNS) & 1)) {
@@ -209,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc::commit(dfull);
         }
+        if (a.sk > 1) split_phases_idle();
     } else {
         // ---------------- decoders / epilogue: thread = weight row = TMEM lane
         const int row = warp * 32 + lane;
@@ -221,20 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint16_t *srow = a.scale + (SMODE == kChannel ? 0 : (int64_t)(rowok ? n : 0) * ngk);
 
         // live chunks c (current), c1 and c2 (codes loaded one and two chunks ahead)
-        int c = next_live(0);
-        int c1 = c < nchunks ? next_live(c + 1) : nchunks;
-        uint4 cur = rowok && c < nchunks ? *reinterpret_cast<const uint4 *>(prow + (size_t)c * 16)
-                                         : make_uint4(0, 0, 0, 0);
-        uint4 nxt = rowok && c1 < nchunks ? *reinterpret_cast<const uint4 *>(prow + (size_t)c1 * 16)
-                                          : make_uint4(0, 0, 0, 0);
+        int c = next_live(cb);
+        int c1 = c < ce ? next_live(c + 1) : ce;
+        uint4 cur = rowok && c < ce ? *reinterpret_cast<const uint4 *>(prow + (size_t)c * 16)
+                                    : make_uint4(0, 0, 0, 0);
+        uint4 nxt = rowok && c1 < ce ? *reinterpret_cast<const uint4 *>(prow + (size_t)c1 * 16)
+                                     : make_uint4(0, 0, 0, 0);
         bool ok = true;
         int lc = 0;  // live chunks decoded
-        for (; c < nchunks; ++lc) {
+        for (; c < ce; ++lc) {
             const int s = lc % C::NA;
             const uint4 codes = cur;
             cur = nxt;
-            const int c2 = c1 < nchunks ? next_live(c1 + 1) : nchunks;
-            if (rowok && c2 < nchunks)
+            const int c2 = c1 < ce ? next_live(c1 + 1) : ce;
+            if (rowok && c2 < ce)
                 nxt = *reinterpret_cast<const uint4 *>(prow + (size_t)c2 * 16);
             uint32_t r[32];
             decode_word_adjacent(codes.x, r + 0);
@@ -297,57 +387,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue
         ok = __all_sync(0xffffffffu, ok);
         bool ready = ok && __all_sync(0xffffffffu, mbar_wait_bounded(dfull, 0));
-        if constexpr (SILU) {
-            // the four epilogue warps exchange values below: decide together
-            volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 2);
-            if (lane == 0) flags[warp] = ready ? 1 : 0;
-            tile_named_bar(1, 128);
-            ready = flags[0] && flags[1] && flags[2] && flags[3];
-            if (!ready && ok) give_up();
-            ok = ok && ready;
-        }
-        if (ready) {
-            tc::fence_after_sync();
-            // channel mode: A held 2*t, so D = 2*sum(t x); group modes: A held t*s
-            float sc = 1.f;
-            if constexpr (SMODE == kChannel) sc = 0.5f * (rowok ? h2f(a.scale[n]) : 0.f);
+        if (a.sk > 1) {
+            split_epilogue(ready, ok, lc, row, n, rowok);
+        } else {
+            if constexpr (SILU) {
+                // the four epilogue warps exchange values below: decide together
+                volatile int *flags = reinterpret_cast<volatile int *>(tmem_slot + 2);
+                if (lane == 0) flags[warp] = ready ? 1 : 0;
+                tile_named_bar(1, 128);
+                ready = flags[0] && flags[1] && flags[2] && flags[3];
+                if (!ready && ok) give_up();
+                ok = ok && ready;
+            }
+            if (ready) {
+                tc::fence_after_sync();
+                // channel mode: A held 2*t, so D = 2*sum(t x); group modes: A held t*s
+                float sc = 1.f;
+                if constexpr (SMODE == kChannel) sc = 0.5f * (rowok ? h2f(a.scale[n]) : 0.f);
 #pragma unroll 1
-            for (int j = 0; j < BN / 32; ++j) {
-                uint32_t d[32];
-                tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
-                tc::wait_ld();
-                if (lc == 0) {  // every chunk of this CTA's rows is a zero block: D was never written
+                for (int j = 0; j < BN / 32; ++j) {
+                    uint32_t d[32];
+                    tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
+                    tc::wait_ld();
+                    if (lc == 0) {  // every chunk of this CTA's rows is a zero block: D was never written
 #pragma unroll
-                    for (int q = 0; q < 32; ++q) d[q] = 0u;
-                }
-                if constexpr (SILU) {
-                    float *ex = reinterpret_cast<float *>(smem);  // [32 tokens][64 pairs]
-                    if (row >= 64) {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) ex[q * 64 + (row - 64)] = __uint_as_float(d[q]) * sc;
+                        for (int q = 0; q < 32; ++q) d[q] = 0u;
                     }
-                    tile_named_bar(1, 128);
-                    if (row < 64 && rowok) {
+                    if constexpr (SILU) {
+                        float *ex = reinterpret_cast<float *>(smem);  // [32 tokens][64 pairs]
+                        if (row >= 64) {
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) ex[q * 64 + (row - 64)] = __uint_as_float(d[q]) * sc;
+                        }
+                        tile_named_bar(1, 128);
+                        if (row < 64 && rowok) {
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) {
+                                const int m = m0 + j * 32 + q;
+                                if (m < a.M)
+                                    OutStore<OUT>::st(a.out, (int64_t)m * a.nh + j0 + row,
+                                                      tile_silu(__uint_as_float(d[q]) * sc) * ex[q * 64 + row]);
+                            }
+                        }
+                        tile_named_bar(1, 128);
+                    } else if (rowok) {
 #pragma unroll
                         for (int q = 0; q < 32; ++q) {
                             const int m = m0 + j * 32 + q;
                             if (m < a.M)
-                                OutStore<OUT>::st(a.out, (int64_t)m * a.nh + j0 + row,
-                                                  tile_silu(__uint_as_float(d[q]) * sc) * ex[q * 64 + row]);
+                                OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, __uint_as_float(d[q]) * sc);
                         }
                     }
-                    tile_named_bar(1, 128);
-                } else if (rowok) {
-#pragma unroll
-                    for (int q = 0; q < 32; ++q) {
-                        const int m = m0 + j * 32 + q;
-                        if (m < a.M)
-                            OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, __uint_as_float(d[q]) * sc);
-                    }
                 }
+            } else if (ok) {
+                give_up();
             }
-        } else if (ok) {
-            give_up();
         }
     }
 
@@ -378,11 +472,97 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// CTAs of one kernel instantiation that a cluster size of sk can keep resident at
+// once, by the driver's occupancy query (which knows shared memory, registers and
+// GPC placement) capped by tensor memory (512 columns per SM).  Cached per device,
+// instantiation and sk.
+template <typename Kern>
+int tile_capacity(Kern kern, int smem, uint32_t tmem_cols, int sk, int sm_count) {
+    static std::mutex mu;
+    static std::map<std::tuple<int, const void *, int>, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_tuple(dev, reinterpret_cast<const void *>(kern), sk);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    const int tmem_cps = (int)(512 / tmem_cols);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+        per_sm = 1;
+    per_sm = per_sm < 1 ? 1 : per_sm;
+    int cap = sm_count * (per_sm < tmem_cps ? per_sm : tmem_cps);
+    if (sk > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, (unsigned)sk);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = (unsigned)sk;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
+            // the query counts shared-memory residency; tensor memory may allow fewer
+            const int64_t ctas = (int64_t)n * sk * (per_sm < tmem_cps ? per_sm : tmem_cps) / per_sm;
+            cap = (int)(ctas < cap ? ctas : cap);
+        } else {
+            cap = 0;  // cluster size not placeable
+        }
+    }
+    cudaGetLastError();
+    cache[key] = cap;
+    return cap;
+}
+
+// Split K for the plain-output tile kernel, considered only when the output tiles
+// alone fill less than one wave.  Cost of a plan, in 64-k chunk times of one CTA:
+// waves * (chunks per CTA + fixed part) * slowdown from SM sharing, where the fixed
+// part covers set-up, pipeline fill and the epilogue (more with the cluster
+// exchange) and CTAs sharing an SM each run ~1.5x slower.
+template <typename Kern>
+void plan_tile_split(Kern kern, int smem, uint32_t tmem_cols, int bn, TileArgs &a, int sm_count) {
+    const int nchunks = a.K / kKC;
+    a.sk = 1;
+    a.cpc = nchunks;
+    static const int force = [] {
+        const char *e = getenv("TERNARY_TILE_SK");
+        return e ? atoi(e) : 0;
+    }();
+    const int64_t tiles = (int64_t)((a.N + 127) / 128) * ((a.M + bn - 1) / bn);
+    const int cap1 = tile_capacity(kern, smem, tmem_cols, 1, sm_count);
+    const int per_sm = cap1 >= sm_count && sm_count > 0 ? cap1 / sm_count : 1;  // CTAs per SM
+    if (tiles >= cap1 && !force) return;
+    double best = 0.0;
+    for (int sk = 1; sk <= 8; sk *= 2) {
+        if (sk > nchunks || bn / sk < 8) break;
+        if (force && sk != force) continue;
+        const int cap = tile_capacity(kern, smem, tmem_cols, sk, sm_count);
+        if (cap < sk) continue;
+        const int cpc = (nchunks + sk - 1) / sk;
+        const int64_t total = tiles * sk;
+        const int64_t waves = (total + cap - 1) / cap;
+        const double sms = (double)cap / per_sm;                      // SMs the clusters use
+        const double load = (double)(total < cap ? total : cap) / sms;  // CTAs per SM in a wave
+        const double share = load > 1.0 ? 1.0 + 0.5 * (load - 1.0) : 1.0;
+        const double cost = (double)waves * (cpc + (sk > 1 ? 6.0 : 4.0)) * share;
+        if (best == 0.0 || cost < best * 0.97) {
+            best = cost;
+            a.sk = sk;
+            a.cpc = cpc;
+        }
+    }
+}
+
 template <int BN, bool BF, int SMODE, int OUT, bool SILU>
-cudaError_t launch_one(const TileArgs &a, cudaStream_t st, bool pdl) {
+cudaError_t launch_one(const TileArgs &a_in, int sm_count, cudaStream_t st, bool pdl) {
     using C = TileCfg<BN, SMODE>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    TileArgs a = a_in;
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
@@ -394,15 +574,26 @@ cudaError_t launch_one(const TileArgs &a, cudaStream_t st, bool pdl) {
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     auto kern = tile_tc_kernel<BN, BF, SMODE, OUT, SILU>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_REQ);
     if (e != cudaSuccess) return e;
+    a.sk = 1;
+    a.cpc = a.K / kKC;
+    if constexpr (!SILU) plan_tile_split(kern, C::SMEM_REQ, C::TMEM_COLS, BN, a, sm_count);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((a.N + 127) / 128), (unsigned)((a.M + BN - 1) / BN), 1);
+    cfg.gridDim = dim3((unsigned)((a.N + 127) / 128), (unsigned)((a.M + BN - 1) / BN), (unsigned)a.sk);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.dynamicSmemBytes = C::SMEM_REQ;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int na = 0;
+    if (a.sk > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = 1;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = (unsigned)a.sk;
+        ++na;
+    }
     if (pdl) {
         attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[na].val.programmaticStreamSerializationAllowed = 1;
@@ -414,33 +605,33 @@ cudaError_t launch_one(const TileArgs &a, cudaStream_t st, bool pdl) {
 }
 
 template <int BN, bool BF, int SMODE, bool SILU>
-cudaError_t launch_out(const TileArgs &a, int out_dtype, cudaStream_t st, bool pdl) {
+cudaError_t launch_out(const TileArgs &a, int out_dtype, int sm_count, cudaStream_t st, bool pdl) {
     switch (out_dtype) {
-    case 0: return launch_one<BN, BF, SMODE, 0, SILU>(a, st, pdl);
-    case 1: return launch_one<BN, BF, SMODE, 1, SILU>(a, st, pdl);
-    default: return launch_one<BN, BF, SMODE, 2, SILU>(a, st, pdl);
+    case 0: return launch_one<BN, BF, SMODE, 0, SILU>(a, sm_count, st, pdl);
+    case 1: return launch_one<BN, BF, SMODE, 1, SILU>(a, sm_count, st, pdl);
+    default: return launch_one<BN, BF, SMODE, 2, SILU>(a, sm_count, st, pdl);
     }
 }
 
 template <int BN, bool SILU>
-cudaError_t launch_bn(const TileArgs &a, bool bf, bool group, int out_dtype, cudaStream_t st,
-                      bool pdl) {
+cudaError_t launch_bn(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
+                      cudaStream_t st, bool pdl) {
     if (!group)
-        return bf ? launch_out<BN, true, kChannel, SILU>(a, out_dtype, st, pdl)
-                  : launch_out<BN, false, kChannel, SILU>(a, out_dtype, st, pdl);
-    return bf ? launch_out<BN, true, kSplit, SILU>(a, out_dtype, st, pdl)
-              : launch_out<BN, false, kFold, SILU>(a, out_dtype, st, pdl);
+        return bf ? launch_out<BN, true, kChannel, SILU>(a, out_dtype, sm_count, st, pdl)
+                  : launch_out<BN, false, kChannel, SILU>(a, out_dtype, sm_count, st, pdl);
+    return bf ? launch_out<BN, true, kSplit, SILU>(a, out_dtype, sm_count, st, pdl)
+              : launch_out<BN, false, kFold, SILU>(a, out_dtype, sm_count, st, pdl);
 }
 
 inline int tile_bn_for(int64_t M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
 
 template <bool SILU>
-cudaError_t launch_tile_any(const TileArgs &a, bool bf, bool group, int out_dtype, cudaStream_t st,
-                            bool pdl) {
+cudaError_t launch_tile_any(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
+                            cudaStream_t st, bool pdl) {
     switch (tile_bn_for(a.M)) {
-    case 64: return launch_bn<64, SILU>(a, bf, group, out_dtype, st, pdl);
-    case 128: return launch_bn<128, SILU>(a, bf, group, out_dtype, st, pdl);
-    default: return launch_bn<256, SILU>(a, bf, group, out_dtype, st, pdl);
+    case 64: return launch_bn<64, SILU>(a, bf, group, out_dtype, sm_count, st, pdl);
+    case 128: return launch_bn<128, SILU>(a, bf, group, out_dtype, sm_count, st, pdl);
+    default: return launch_bn<256, SILU>(a, bf, group, out_dtype, sm_count, st, pdl);
     }
 }
 
