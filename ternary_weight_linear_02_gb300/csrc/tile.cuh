@@ -41,9 +41,10 @@
 //    -- the sum is the same on every run -- then scales and stores.  Fills the
 //    GPU when ceil(N/128) * ceil(M/BN) tiles alone would leave SMs idle.
 //  * SiLU-gated mode (SILU = true, a stacked gate/up layer): the CTA's 128 rows
-//    are 64 gate rows and the matching 64 up rows; in the epilogue the up lanes
-//    pass their scaled values through shared memory (the x ring, idle once D is
-//    complete) and the gate lanes write out[m, j] = silu(g) * u.
+//    are 64 gate rows and the matching 64 up rows; in the epilogue every lane
+//    writes its scaled row to shared memory (the x ring, idle once D is
+//    complete), and after one barrier the 128 threads split the (pair, token)
+//    outputs out[m, j] = silu(g) * u between them.
 // Every mbarrier wait is bounded; a wait that gives up sets the device status
 // word, the CTA stops issuing work, frees its TMEM and returns.
 #pragma once
@@ -191,10 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         cl_arrive_release();  // phase 1: every CTA's D is final (or given up), its x ring idle
         cl_wait_acquire();
         const bool cta_ok = !*abort_flag && wready[0] && wready[1] && wready[2] && wready[3];
-        const int sk = a.sk, slice = BN / sk, lsl = 31 - __clz(slice);
-        // receive buffer [source rank][slice column][128 rows] fp32 = 512 * BN bytes,
-        // the size of the x ring; lanes write consecutive rows (no bank conflicts)
-        const float *recv = reinterpret_cast<const float *>(smem);
+        const int sk = a.sk, slice = BN / sk, lsl = 31 - __clz(slice), g4 = slice >> 2;
+        // receive buffer [source rank][slice column / 4][128 rows][4] fp32 = 512 * BN
+        // bytes, the size of the x ring: one 16-byte store per 4 columns, lanes write
+        // consecutive rows (no bank conflicts)
+        const float4 *recv = reinterpret_cast<const float4 *>(smem);
         const uint32_t recv_u32 = smem_u32(smem);
         if (cta_ok) {
             tc::fence_after_sync();
@@ -203,13 +205,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t d[32];
                 tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
                 tc::wait_ld();
+                if (lc == 0) {  // no live chunk in this CTA's range: D was never written
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int q = j * 32 + i;  // token column of the tile
+                    for (int i = 0; i < 32; ++i) d[i] = 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const int q = j * 32 + i;  // token column of the tile (slice holds whole 4s)
                     const uint32_t off =
-                        ((((uint32_t)krank << lsl) + (uint32_t)(q & (slice - 1))) * 128u + (uint32_t)row) * 4u;
-                    // lc == 0: no live chunk in this CTA's range, D was never written
-                    cl_st_f32(cl_map(recv_u32 + off, (uint32_t)(q >> lsl)), lc == 0 ? 0.f : __uint_as_float(d[i]));
+                        ((uint32_t)(krank * g4 + ((q & (slice - 1)) >> 2)) * 128u + (uint32_t)row) * 16u;
+                    cl_st_v4_f32(cl_map(recv_u32 + off, (uint32_t)(q >> lsl)), __uint_as_float(d[i]),
+                                 __uint_as_float(d[i + 1]), __uint_as_float(d[i + 2]), __uint_as_float(d[i + 3]));
                 }
             }
         }
@@ -226,10 +232,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sc = 1.f;
         if constexpr (SMODE == kChannel) sc = 0.5f * h2f(a.scale[n]);
         const int mb = m0 + krank * slice;
-        for (int c = 0; c < slice && mb + c < a.M; ++c) {
-            float v = 0.f;
-            for (int r = 0; r < sk; ++r) v += recv[((r << lsl) + c) * 128 + row];
-            OutStore<OUT>::st(a.out, (int64_t)(mb + c) * a.N + n, v * sc);
+        for (int c4 = 0; c4 < g4 && mb + 4 * c4 < a.M; ++c4) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < sk; ++r) {
+                const float4 p = recv[(r * g4 + c4) * 128 + row];
+                v.x += p.x;
+                v.y += p.y;
+                v.z += p.z;
+                v.w += p.w;
+            }
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (mb + 4 * c4 + e < a.M) OutStore<OUT>::st(a.out, (int64_t)(mb + 4 * c4 + e) * a.N + n, vv[e] * sc);
         }
     };
 
@@ -404,38 +419,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // channel mode: A held 2*t, so D = 2*sum(t x); group modes: A held t*s
                 float sc = 1.f;
                 if constexpr (SMODE == kChannel) sc = 0.5f * (rowok ? h2f(a.scale[n]) : 0.f);
+                if constexpr (SILU) {
+                    // every row's scaled values go to shared memory (the idle x ring,
+                    // [token][128 rows] fp32 = 512 * BN bytes); after one barrier thread
+                    // t writes pair p = t % 64 for half t / 64 of the tokens:
+                    // out[m, j0 + p] = silu(gate) * up
+                    float *ex = reinterpret_cast<float *>(smem);
 #pragma unroll 1
-                for (int j = 0; j < BN / 32; ++j) {
-                    uint32_t d[32];
-                    tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
-                    tc::wait_ld();
-                    if (lc == 0) {  // every chunk of this CTA's rows is a zero block: D was never written
+                    for (int j = 0; j < BN / 32; ++j) {
+                        uint32_t d[32];
+                        tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
+                        tc::wait_ld();
 #pragma unroll
-                        for (int q = 0; q < 32; ++q) d[q] = 0u;
+                        for (int q = 0; q < 32; ++q)  // lc == 0: every chunk a zero block, D never written
+                            ex[(j * 32 + q) * 128 + row] = lc == 0 ? 0.f : __uint_as_float(d[q]) * sc;
                     }
-                    if constexpr (SILU) {
-                        float *ex = reinterpret_cast<float *>(smem);  // [32 tokens][64 pairs]
-                        if (row >= 64) {
+                    tile_named_bar(1, 128);
+                    const int p = row & 63, q0 = (row >> 6) * (BN / 2);
+                    if (j0 + p < a.nh) {
+#pragma unroll 4
+                        for (int q = q0; q < q0 + BN / 2 && m0 + q < a.M; ++q)
+                            OutStore<OUT>::st(a.out, (int64_t)(m0 + q) * a.nh + j0 + p,
+                                              tile_silu(ex[q * 128 + p]) * ex[q * 128 + 64 + p]);
+                    }
+                } else {
+#pragma unroll 1
+                    for (int j = 0; j < BN / 32; ++j) {
+                        uint32_t d[32];
+                        tc::ld_32x32b_x32(dcol + ((uint32_t)(warp * 32) << 16) + (uint32_t)(j * 32), d);
+                        tc::wait_ld();
+                        if (lc == 0) {  // every chunk of this CTA's rows is a zero block: D was never written
 #pragma unroll
-                            for (int q = 0; q < 32; ++q) ex[q * 64 + (row - 64)] = __uint_as_float(d[q]) * sc;
+                            for (int q = 0; q < 32; ++q) d[q] = 0u;
                         }
-                        tile_named_bar(1, 128);
-                        if (row < 64 && rowok) {
+                        if (rowok) {
 #pragma unroll
                             for (int q = 0; q < 32; ++q) {
                                 const int m = m0 + j * 32 + q;
                                 if (m < a.M)
-                                    OutStore<OUT>::st(a.out, (int64_t)m * a.nh + j0 + row,
-                                                      tile_silu(__uint_as_float(d[q]) * sc) * ex[q * 64 + row]);
+                                    OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, __uint_as_float(d[q]) * sc);
                             }
-                        }
-                        tile_named_bar(1, 128);
-                    } else if (rowok) {
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const int m = m0 + j * 32 + q;
-                            if (m < a.M)
-                                OutStore<OUT>::st(a.out, (int64_t)m * a.N + n, __uint_as_float(d[q]) * sc);
                         }
                     }
                 }
@@ -518,11 +541,13 @@ int tile_capacity(Kern kern, int smem, uint32_t tmem_cols, int sk, int sm_count)
     return cap;
 }
 
-// Split K for the plain-output tile kernel, considered only when the output tiles
-// alone fill less than one wave.  Cost of a plan, in 64-k chunk times of one CTA:
-// waves * (chunks per CTA + fixed part) * slowdown from SM sharing, where the fixed
-// part covers set-up, pipeline fill and the epilogue (more with the cluster
-// exchange) and CTAs sharing an SM each run ~1.5x slower.
+// Split K for the plain-output tile kernel.  Cost of a plan, in 64-k chunk times of
+// one CTA (fitted to per-layer timings of the 7B stack's shapes at M = 64, 256 and
+// 2048):  waves * (chunks per CTA + O + E [split]) * sharing, where O is a CTA's
+// fixed time (set-up, pipeline fill, epilogue: ~18 chunks at BN = 256, ~12 at
+// BN <= 128), E the cluster exchange (~8 at BN = 256, ~3 at BN = 64), waves come
+// from the occupancy query, and an SM running two CTAs at once takes ~1.4x as long
+// as one.
 template <typename Kern>
 void plan_tile_split(Kern kern, int smem, uint32_t tmem_cols, int bn, TileArgs &a, int sm_count) {
     const int nchunks = a.K / kKC;
@@ -535,7 +560,8 @@ void plan_tile_split(Kern kern, int smem, uint32_t tmem_cols, int bn, TileArgs &
     const int64_t tiles = (int64_t)((a.N + 127) / 128) * ((a.M + bn - 1) / bn);
     const int cap1 = tile_capacity(kern, smem, tmem_cols, 1, sm_count);
     const int per_sm = cap1 >= sm_count && sm_count > 0 ? cap1 / sm_count : 1;  // CTAs per SM
-    if (tiles >= cap1 && !force) return;
+    const double O = bn >= 256 ? 18.0 : 12.0;
+    const double E = 3.0 + 5.0 * (bn - 64) / 192.0;
     double best = 0.0;
     for (int sk = 1; sk <= 8; sk *= 2) {
         if (sk > nchunks || bn / sk < 8) break;
@@ -545,10 +571,11 @@ void plan_tile_split(Kern kern, int smem, uint32_t tmem_cols, int bn, TileArgs &
         const int cpc = (nchunks + sk - 1) / sk;
         const int64_t total = tiles * sk;
         const int64_t waves = (total + cap - 1) / cap;
-        const double sms = (double)cap / per_sm;                      // SMs the clusters use
-        const double load = (double)(total < cap ? total : cap) / sms;  // CTAs per SM in a wave
-        const double share = load > 1.0 ? 1.0 + 0.5 * (load - 1.0) : 1.0;
-        const double cost = (double)waves * (cpc + (sk > 1 ? 6.0 : 4.0)) * share;
+        const int64_t sms = cap / per_sm;  // SMs the clusters reach
+        const int64_t in_wave = total < cap ? total : cap;
+        const int64_t load = (in_wave + sms - 1) / sms;  // CTAs on the busiest SM
+        const double share = 1.0 + 0.4 * (double)(load - 1);
+        const double cost = (double)waves * (cpc + O + (sk > 1 ? E : 0.0)) * share;
         if (best == 0.0 || cost < best * 0.97) {
             best = cost;
             a.sk = sk;
