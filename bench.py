@@ -245,6 +245,15 @@ def per_m_entry(cfg, M, ms, pk, calls):
     return e
 
 
+def kernel_of(M):
+    """The kernel family the automatic dispatch runs at M (K % 64 == 0)."""
+    if M <= 16:
+        return "decode kernel (warp MMAs, TMA-staged weights)"
+    if M <= 32:
+        return "tcgen05 skinny kernel"
+    return "tcgen05 tile kernel"
+
+
 def roofline_of(cfg, M, ms, pk, pk_src, traffic):
     """The roofline object for the pass at M: every launch of one pass is the same
     kernel family, so per-launch work / average launch time = pass work / pass time."""
@@ -255,14 +264,14 @@ def roofline_of(cfg, M, ms, pk, pk_src, traffic):
         peak = pk["bf16_tflops"]
         return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "traffic": traffic, "M": M,
-                "kernel": f"tile kernel, every launch of the M={M} pass ({calls} launches)",
+                "kernel": f"{kernel_of(M)}, every launch of the M={M} pass ({calls} launches)",
                 "peak_note": f"bf16_tflops (burst) of {pk_src} peaks; "
                              f"{ach / pk['bf16_tflops_sustained']:.3f} of the sustained figure"}
     ach = algorithmic_bytes(cfg, M) / t / 1e9
     peak = pk["hbm_gbs"]
     return {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s", "frac": ach / peak,
             "traffic": traffic, "M": M,
-            "kernel": f"decode kernel, every launch of the M={M} pass ({calls} launches)",
+            "kernel": f"{kernel_of(M)}, every launch of the M={M} pass ({calls} launches)",
             "peak_note": f"hbm_gbs of {pk_src} peaks"}
 
 

@@ -8,7 +8,9 @@ finished and only waits for it before reading x and writing out.  Here a
 product, down reading that product, the next layer's o reading down's output --
 is captured, replayed twice, and every call's output is compared with the
 oracle evaluated on that call's actual input.  The shapes need split K and more
-CTAs than one per SM, so CTAs of neighbouring kernels share SMs.
+CTAs than one per SM, so CTAs of neighbouring kernels share SMs.  M = 1, 4, 16
+run the decode kernel, M = 24 the tcgen05 skinny kernel, M = 64 and 300 the
+tile kernel with split-K clusters.
 """
 import numpy as np
 import pytest
@@ -44,7 +46,7 @@ def weights(d, name, N, K, gs):
 
 
 @pytest.mark.parametrize("gs", [0, 128])
-@pytest.mark.parametrize("M", [1, 4, 16])
+@pytest.mark.parametrize("M", [1, 4, 16, 24, 64, 300])
 def test_static_weight_chain_graph(M, gs):
     dt = torch.bfloat16
     W = [{"qkv": weights(d, "qkv", N_QKV, K_HID, gs), "o": weights(d, "o", K_HID, K_HID, gs),
