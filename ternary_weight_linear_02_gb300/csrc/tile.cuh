@@ -64,7 +64,6 @@ namespace tl {
 namespace {
 
 constexpr int kKC = 64;   // k per pipeline chunk = one 128-byte row of x
-constexpr int kNS = 4;    // x stages in shared memory
 constexpr int kThreads = 192;
 
 enum { kChannel = 0, kFold = 1, kSplit = 2 };
@@ -77,13 +76,23 @@ __host__ __device__ constexpr uint32_t pow2ceil(uint32_t v) {
 
 template <int BN, int SMODE>
 struct TileCfg {
-    static constexpr int ACOLS = (SMODE == kSplit) ? 64 : 32;  // TMEM columns per A stage
-    static constexpr int NA = (SMODE == kSplit) ? 3 : 4;       // A stages
-    static constexpr uint32_t TMEM_COLS = pow2ceil(NA * ACOLS + BN);
-    static constexpr int XSTAGE = BN * 128;                    // bytes per x stage
+    // A pipeline stage holds CPS consecutive live 64-k chunks: one round of
+    // barrier waits and commits per stage.  Measured: the hand-offs of a round,
+    // not the MMA rate, bounded the loop at one chunk per round (twice the MMAs per
+    // round cost 1.37x the time), so the 256-token tiles take two chunks per round.
+    static constexpr int CPS = (BN == 256) ? 2 : 1;
+    static constexpr int ACOLS = (SMODE == kSplit) ? 64 : 32;  // TMEM columns per chunk of A
+    // A stages: at BN = 256 they fill the 256 TMEM columns next to D; smaller tiles
+    // keep four (three with split scales), deeper rings measured ~4% slower there
+    static constexpr int NA = (BN == 256) ? 256 / (ACOLS * CPS) : (SMODE == kSplit ? 3 : 4);
+    static constexpr uint32_t TMEM_COLS = pow2ceil(NA * ACOLS * CPS + BN);
+    static constexpr int NS = (BN == 256) ? 3 : 4;  // x stages
+    static constexpr int XCHUNK = BN * 128;                    // bytes of x per 64-k chunk
+    static constexpr int XSTAGE = CPS * XCHUNK;                // bytes per x stage
+    static_assert(NS * XSTAGE >= 4 * XCHUNK, "x ring holds the epilogue exchanges (512 * BN bytes)");
     // shared memory: [x stages][barriers][tmem slot, abort flag] + 1 KB alignment slack
-    static constexpr int BAR_OFF = kNS * XSTAGE;
-    static constexpr int NBARS = 2 * kNS + 2 * NA + 1;
+    static constexpr int BAR_OFF = NS * XSTAGE;
+    static constexpr int NBARS = 2 * NS + 2 * NA + 1;
     // [tmem slot, abort flag, four epilogue flags, -, -, eight split-K rank flags]
     // after the barriers
     static constexpr int SMEM = BAR_OFF + NBARS * 8 + 64 + 1024;
@@ -130,8 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::BAR_OFF);
-    uint64_t *xfull = bars, *xempty = bars + kNS;
-    uint64_t *afull = bars + 2 * kNS, *aempty = afull + C::NA;
+    uint64_t *xfull = bars, *xempty = bars + C::NS;
+    uint64_t *afull = bars + 2 * C::NS, *aempty = afull + C::NA;
     uint64_t *dfull = aempty + C::NA;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -146,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb = min(nchunks, krank * a.cpc), ce = a.sk > 1 ? min(nchunks, cb + a.cpc) : nchunks;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kNS; ++i) {
+        for (int i = 0; i < C::NS; ++i) {
             mbar_init(&xfull[i], 1);
             mbar_init(&xempty[i], 1);
         }
@@ -163,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t dcol = tmem + (uint32_t)(C::NA * C::ACOLS);
+    const uint32_t dcol = tmem + (uint32_t)(C::NA * C::CPS * C::ACOLS);
 
     pdl_launch_dependents();
     pdl_wait();  // x / packed / out may be produced / consumed by the previous kernel
@@ -276,14 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tc::prefetch_tmap(&tmx);
             int lc = 0;  // live chunks issued
-            for (int c = next_live(cb); c < ce && !*abort_flag; c = next_live(c + 1), ++lc) {
-                const int s = lc % kNS;
-                if (lc >= kNS && !mbar_wait_bounded(&xempty[s], ((lc / kNS) - 1) & 1)) {
-                    give_up();
-                    break;
+            for (int c = next_live(cb); c < ce && !*abort_flag; ++lc) {
+                const int cn = next_live(c + 1);
+                const int st = lc / C::CPS, h = lc % C::CPS, s = st % C::NS;
+                if (h == 0) {
+                    if (st >= C::NS && !mbar_wait_bounded(&xempty[s], ((st / C::NS) - 1) & 1)) {
+                        give_up();
+                        break;
+                    }
+                    // one arrival per stage, expecting every chunk the stage will hold
+                    const int nch = (C::CPS == 2 && cn < ce) ? 2 : 1;
+                    mbar_arrive_expect_tx(&xfull[s], (uint32_t)(nch * C::XCHUNK));
                 }
-                mbar_arrive_expect_tx(&xfull[s], (uint32_t)C::XSTAGE);
-                tc::tma_load_2d(smem + (size_t)s * C::XSTAGE, &tmx, c * kKC, m0, &xfull[s]);
+                tc::tma_load_2d(smem + (size_t)s * C::XSTAGE + (size_t)h * C::XCHUNK, &tmx, c * kKC, m0,
+                                &xfull[s]);
+                c = cn;
             }
         }
         if (a.sk > 1) split_phases_idle();
@@ -292,21 +308,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc = tc::idesc_f16(BN, BF);
             int lc = 0;  // live chunks multiplied
-            for (int c = next_live(cb); c < ce; c = next_live(c + 1), ++lc) {
-                const int s = lc % C::NA, xs = lc % kNS;
-                if (*abort_flag || !mbar_wait_bounded(&afull[s], (lc / C::NA) & 1) ||
-                    !mbar_wait_bounded(&xfull[xs], (lc / kNS) & 1)) {
+            for (int c = next_live(cb), st = 0; c < ce; ++st) {
+                const int s = st % C::NA, xs = st % C::NS;
+                if (*abort_flag || !mbar_wait_bounded(&afull[s], (st / C::NA) & 1) ||
+                    !mbar_wait_bounded(&xfull[xs], (st / C::NS) & 1)) {
                     give_up();
                     break;
                 }
                 tc::fence_after_sync();
-                const uint64_t bdesc = tc::desc_sw128(smem + (size_t)xs * C::XSTAGE);
-                const uint32_t acol = tmem + (uint32_t)(s * C::ACOLS);
+                for (int h = 0; h < C::CPS && c < ce; ++h, ++lc, c = next_live(c + 1)) {
+                    const uint64_t bdesc = tc::desc_sw128(smem + (size_t)xs * C::XSTAGE + (size_t)h * C::XCHUNK);
+                    const uint32_t acol = tmem + (uint32_t)((s * C::CPS + h) * C::ACOLS);
 #pragma unroll
-                for (int kk = 0; kk < kKC / 16; ++kk) {
-                    const uint64_t b = bdesc + (uint64_t)(kk * 2);  // +32 B per 16 elements
-                    tc::mma_ts(dcol, acol + kk * 8, b, idesc, (lc | kk) != 0);
-                    if constexpr (SMODE == kSplit) tc::mma_ts(dcol, acol + 32 + kk * 8, b, idesc, 1);
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const uint64_t b = bdesc + (uint64_t)(kk * 2);  // +32 B per 16 elements
+                        tc::mma_ts(dcol, acol + kk * 8, b, idesc, (lc | kk) != 0);
+                        if constexpr (SMODE == kSplit) tc::mma_ts(dcol, acol + 32 + kk * 8, b, idesc, 1);
+                    }
                 }
                 tc::commit(&aempty[s]);
                 tc::commit(&xempty[xs]);
@@ -335,7 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         int lc = 0;  // live chunks decoded
         for (; c < ce; ++lc) {
-            const int s = lc % C::NA;
+            // stage st = lc / CPS holds this chunk in half h; the A ring is waited for
+            // at a stage's first chunk and handed to the issuer after its last
+            const int st = lc / C::CPS, h = lc % C::CPS, s = st % C::NA;
+            const bool stage_end = (h == C::CPS - 1) || c1 >= ce;
             const uint4 codes = cur;
             cur = nxt;
             const int c2 = c1 < ce ? next_live(c1 + 1) : ce;
@@ -384,18 +405,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // wait results are made warp-uniform: tcgen05.st below is warp-collective
-            if (lc >= C::NA) ok = __all_sync(0xffffffffu, mbar_wait_bounded(&aempty[s], ((lc / C::NA) - 1) & 1));
+            if (h == 0 && st >= C::NA)
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&aempty[s], ((st / C::NA) - 1) & 1));
             if (!ok) give_up();
             if (__any_sync(0xffffffffu, !ok || *abort_flag)) {
                 ok = false;
                 break;
             }
-            tc::st_32x32b_x32(tlane + (uint32_t)(s * C::ACOLS), r);
-            if constexpr (SMODE == kSplit) tc::st_32x32b_x32(tlane + (uint32_t)(s * C::ACOLS + 32), rl);
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[s]);
+            const uint32_t acol = tlane + (uint32_t)((s * C::CPS + h) * C::ACOLS);
+            tc::st_32x32b_x32(acol, r);
+            if constexpr (SMODE == kSplit) tc::st_32x32b_x32(acol + 32, rl);
+            if (stage_end) {
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[s]);
+            }
             c = c1;
             c1 = c2;
         }
