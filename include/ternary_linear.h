@@ -264,6 +264,13 @@ void ternary_test_inject_launch_failures(int32_t n);
  * without a fault or a hang. */
 void ternary_test_set_wait_limit(int64_t cycles, int32_t stall);
 
+/* Testing aid: the form of the tile kernel for every later call that runs on
+ * it: 0 = chosen per call by the library (default), 1 = one output tile per
+ * CTA (with split K where planned), 2 = persistent CTAs (one per SM, each
+ * walking a list of 128-row x 192-token tiles).  Both forms compute the same
+ * sums; any other value restores 0.  Lets tests cover both forms on any shape. */
+void ternary_test_set_tile_mode(int32_t mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -82,6 +82,8 @@ def load():
     lib.ternary_test_inject_launch_failures.restype = None
     lib.ternary_test_set_wait_limit.argtypes = [i64, i32]
     lib.ternary_test_set_wait_limit.restype = None
+    lib.ternary_test_set_tile_mode.argtypes = [i32]
+    lib.ternary_test_set_tile_mode.restype = None
     lib.ternary_device_status_async.argtypes = [p, i32, p]
     lib.ternary_device_status_async.restype = ctypes.c_int
     lib.ternary_block_mask_words.argtypes = [i64, i64]

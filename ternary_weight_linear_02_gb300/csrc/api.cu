@@ -28,6 +28,9 @@ std::atomic<int> g_inject_launch_failures{0};
 // testing aids for the decode kernel's bounded waits (ternary_test_set_wait_limit)
 std::atomic<long long> g_wait_limit{0};  // 0 = the default (~0.5 s)
 std::atomic<int> g_stall{0};
+// testing aid: the tile kernel's form (ternary_test_set_tile_mode): 0 = chosen
+// per call, 1 = one tile per CTA, 2 = persistent CTAs
+std::atomic<int> g_tile_mode{0};
 
 int env_int(const char *name, int dflt) {
     const char *v = std::getenv(name);
@@ -311,6 +314,7 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     a.status = d->status;
     a.mask = mask;
     a.mask_words = tl::mask_words(K);
+    a.persist = g_tile_mode.load() - 1;
     return from_cuda(tl::launch_tile(a, bf, group, out_dtype, d->sm_count, st, pdl_enabled()));
 }
 
@@ -395,7 +399,8 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     a.status = d->status;
     a.mask = mask;
     a.mask_words = tl::mask_words(K);
-    return from_cuda(tl::launch_tile_silu(a, bf, group, out_dtype, st, pdl_enabled()));
+    a.persist = g_tile_mode.load() - 1;
+    return from_cuda(tl::launch_tile_silu(a, bf, group, out_dtype, d->sm_count, st, pdl_enabled()));
 }
 
 tl_status check_packing(const void *t, const void *packed, int64_t N, int64_t K,
@@ -567,6 +572,8 @@ void ternary_test_set_wait_limit(int64_t cycles, int32_t stall) {
     g_wait_limit.store(cycles > 0 ? cycles : 0);
     g_stall.store(stall ? 1 : 0);
 }
+
+void ternary_test_set_tile_mode(int32_t mode) { g_tile_mode.store(mode == 1 || mode == 2 ? mode : 0); }
 
 tl_status ternary_device_status_async(int32_t *dst, int32_t clear, void *stream) {
     if (dst == nullptr) return TL_ERR_NULL;

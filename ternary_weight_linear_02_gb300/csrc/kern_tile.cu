@@ -1,6 +1,6 @@
 // kern_tile.cu -- large-M ternary linear on the tensor cores: support check and
 // the plain-output entry point.  The kernel itself is in tile.cuh.
-#include "tile.cuh"
+#include "tile_persist.cuh"
 
 namespace tl {
 
@@ -10,8 +10,31 @@ bool tile_supported(int64_t M, int64_t N, int64_t K) {
            encode_fn() != nullptr;
 }
 
+// The persistent form takes large-M calls whose tiles it spreads more evenly over
+// the SMs, or whose per-tile fixed time it hides, than one tile per CTA does.
+// Costs in 64-k chunk times of a 256-token tile (fitted to the 7B shapes at
+// M = 2048): one tile per CTA = waves x (chunks + 18) (+8 per split-K exchange,
+// +6 for the gated epilogue); persistent = busiest CTA's tiles x (chunks + 2) x
+// P192 + 18, P192 the measured time of a 192-token chunk relative to a 256-token one.
+bool use_persist(const TileArgs &a, bool silu, int sm_count) {
+    if (a.persist >= 0) return a.persist == 1;
+    if (a.M <= 256 || sm_count <= 0) return false;
+    const int64_t rb = silu ? (a.nh + 63) / 64 : (a.N + 127) / 128;
+    const int nch = a.K / 64;
+    double classic = 0.0;
+    const int64_t tiles256 = rb * ((a.M + 255) / 256);
+    for (int sk = 1; sk <= (silu ? 1 : 2); ++sk) {
+        const int64_t waves = (tiles256 * sk + sm_count - 1) / sm_count;
+        const double c = (double)waves * ((nch + sk - 1) / sk + 18.0 + (sk > 1 ? 8.0 : 0.0) + (silu ? 6.0 : 0.0));
+        if (classic == 0.0 || c < classic) classic = c;
+    }
+    return persist_cost(a, silu, sm_count) < classic;
+}
+
 cudaError_t launch_tile(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
                         cudaStream_t st, bool pdl) {
+    if (use_persist(a, false, sm_count))
+        return launch_persist<false>(a, bf, group, out_dtype, sm_count, st, pdl);
     return launch_tile_any<false>(a, bf, group, out_dtype, sm_count, st, pdl);
 }
 

@@ -161,13 +161,14 @@ struct TileArgs {
     int mask_words;          // map words per 128-row block
     int sk;                  // K split = cluster size along grid z (set by the launcher)
     int cpc;                 // 64-k chunks per CTA of the split (set by the launcher)
+    int persist;             // -1: the launcher decides; 0: one tile per CTA; 1: persistent CTAs
 };
 
 bool tile_supported(int64_t M, int64_t N, int64_t K);  // K % 64 == 0
 cudaError_t launch_tile(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
                         cudaStream_t st, bool pdl);
 // SiLU-gated gate/up product on the tile kernel: a.N = 2 * a.nh stacked rows, out [M, nh]
-cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype,
+cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
                              cudaStream_t st, bool pdl);
 
 // ------------------------------------------------------------ generic path (K % 64 != 0)
