@@ -50,6 +50,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <stdio.h>
 #include <stdlib.h>
 
 #include <map>
@@ -79,14 +80,18 @@ struct TileCfg {
     // A pipeline stage holds CPS consecutive live 64-k chunks: one round of
     // barrier waits and commits per stage.  Measured: the hand-offs of a round,
     // not the MMA rate, bounded the loop at one chunk per round (twice the MMAs per
-    // round cost 1.37x the time), so the 256-token tiles take two chunks per round.
-    static constexpr int CPS = (BN == 256) ? 2 : 1;
+    // round cost 1.37x the time), so stages take two chunks -- except for split
+    // scales on the smaller tiles, whose 64-column chunks would leave one A stage
+    // in the 256 columns of a two-CTA-per-SM allocation.
+    static constexpr int CPS = (BN == 256 || SMODE != kSplit) ? 2 : 1;
     static constexpr int ACOLS = (SMODE == kSplit) ? 64 : 32;  // TMEM columns per chunk of A
     // A stages: at BN = 256 they fill the 256 TMEM columns next to D; smaller tiles
-    // keep four (three with split scales), deeper rings measured ~4% slower there
-    static constexpr int NA = (BN == 256) ? 256 / (ACOLS * CPS) : (SMODE == kSplit ? 3 : 4);
+    // keep the allocation at 256 columns (two CTAs per SM)
+    static constexpr int NA = (BN == 256) ? 256 / (ACOLS * CPS)
+                              : (CPS == 2) ? (BN == 128 ? 2 : 3)
+                                           : (SMODE == kSplit ? 3 : 4);
     static constexpr uint32_t TMEM_COLS = pow2ceil(NA * ACOLS * CPS + BN);
-    static constexpr int NS = (BN == 256) ? 3 : 4;  // x stages
+    static constexpr int NS = (BN == 256 || (BN == 128 && CPS == 2)) ? 3 : 4;  // x stages
     static constexpr int XCHUNK = BN * 128;                    // bytes of x per 64-k chunk
     static constexpr int XSTAGE = CPS * XCHUNK;                // bytes per x stage
     static_assert(NS * XSTAGE >= 4 * XCHUNK, "x ring holds the epilogue exchanges (512 * BN bytes)");
@@ -521,9 +526,12 @@ EncodeTiledFn encode_fn() {
 }
 
 // CTAs of one kernel instantiation that a cluster size of sk can keep resident at
-// once, by the driver's occupancy query (which knows shared memory, registers and
-// GPC placement) capped by tensor memory (512 columns per SM).  Cached per device,
-// instantiation and sk.
+// once.  CTAs per SM come from the kernel's resources -- shared memory (228 KB per
+// SM, 1 KB reserved per CTA), threads, registers and the 512 TMEM columns: the
+// occupancy query assumes the default split of L1 and shared memory and reports
+// one CTA per SM for tiles that measurably run two.  The cluster query adds the
+// GPC placement limit and is scaled by the ratio of the two per-SM counts.
+// Cached per device, instantiation and sk.
 template <typename Kern>
 int tile_capacity(Kern kern, int smem, uint32_t tmem_cols, int sk, int sm_count) {
     static std::mutex mu;
@@ -534,12 +542,22 @@ int tile_capacity(Kern kern, int smem, uint32_t tmem_cols, int sk, int sm_count)
     std::lock_guard<std::mutex> lk(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
-    const int tmem_cps = (int)(512 / tmem_cols);
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
-        per_sm = 1;
+    int per_sm = (int)(512 / tmem_cols);
+    const int by_smem = (228 * 1024) / (smem + 1024), by_threads = 2048 / kThreads;
+    per_sm = by_smem < per_sm ? by_smem : per_sm;
+    per_sm = by_threads < per_sm ? by_threads : per_sm;
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs > 0) {
+        const int warp_regs = ((fa.numRegs * 32 + 255) / 256) * 256;  // allocated per warp
+        const int by_regs = 65536 / (warp_regs * (kThreads / 32));
+        per_sm = by_regs < per_sm ? by_regs : per_sm;
+    }
     per_sm = per_sm < 1 ? 1 : per_sm;
-    int cap = sm_count * (per_sm < tmem_cps ? per_sm : tmem_cps);
+    int api_per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&api_per_sm, kern, kThreads, smem) != cudaSuccess ||
+        api_per_sm < 1)
+        api_per_sm = 1;
+    int cap = sm_count * per_sm;
     if (sk > 1) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(1, 1, (unsigned)sk);
@@ -554,8 +572,7 @@ int tile_capacity(Kern kern, int smem, uint32_t tmem_cols, int sk, int sm_count)
         cfg.numAttrs = 1;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) {
-            // the query counts shared-memory residency; tensor memory may allow fewer
-            const int64_t ctas = (int64_t)n * sk * (per_sm < tmem_cps ? per_sm : tmem_cps) / per_sm;
+            const int64_t ctas = (int64_t)n * sk * per_sm / api_per_sm;
             cap = (int)(ctas < cap ? ctas : cap);
         } else {
             cap = 0;  // cluster size not placeable
@@ -566,8 +583,9 @@ int tile_capacity(Kern kern, int smem, uint32_t tmem_cols, int sk, int sm_count)
     return cap;
 }
 
-// Split K for the plain-output tile kernel.  Cost of a plan, in 64-k chunk times of
-// one CTA (fitted to per-layer timings of the 7B stack's shapes at M = 64, 256 and
+// Split K for the plain-output tile kernel (TERNARY_PLAN_LOG in the environment
+// prints every candidate to stderr).  Cost of a plan, in 64-k chunk times of one
+// CTA (fitted to per-layer timings of the 7B stack's shapes at M = 64, 256 and
 // 2048):  waves * (chunks per CTA + O + E [split]) * sharing, where O is a CTA's
 // fixed time (set-up, pipeline fill, epilogue: ~18 chunks at BN = 256, ~12 at
 // BN <= 128), E the cluster exchange (~8 at BN = 256, ~3 at BN = 64), waves come
@@ -587,6 +605,7 @@ void plan_tile_split(Kern kern, int smem, uint32_t tmem_cols, int bn, TileArgs &
     const int per_sm = cap1 >= sm_count && sm_count > 0 ? cap1 / sm_count : 1;  // CTAs per SM
     const double O = bn >= 256 ? 18.0 : 12.0;
     const double E = 3.0 + 5.0 * (bn - 64) / 192.0;
+    static const bool log = getenv("TERNARY_PLAN_LOG") != nullptr;
     double best = 0.0;
     for (int sk = 1; sk <= 8; sk *= 2) {
         if (sk > nchunks || bn / sk < 8) break;
@@ -601,6 +620,9 @@ void plan_tile_split(Kern kern, int smem, uint32_t tmem_cols, int bn, TileArgs &
         const int64_t load = (in_wave + sms - 1) / sms;  // CTAs on the busiest SM
         const double share = 1.0 + 0.4 * (double)(load - 1);
         const double cost = (double)waves * (cpc + O + (sk > 1 ? E : 0.0)) * share;
+        if (log)
+            fprintf(stderr, "tile plan M=%d N=%d K=%d BN=%d: sk=%d capacity=%d CTAs (%d per SM) waves=%lld cost=%.1f\n",
+                    a.M, a.N, a.K, bn, sk, cap, per_sm, (long long)waves, cost);
         if (best == 0.0 || cost < best * 0.97) {
             best = cost;
             a.sk = sk;
