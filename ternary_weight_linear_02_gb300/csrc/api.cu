@@ -180,6 +180,15 @@ tl_status check_linear(const void *x, int32_t x_dtype, const uint8_t *packed, co
     return TL_OK;
 }
 
+// Decode shapes that the tcgen05 skinny kernel serves faster than the register-fed
+// decode kernel (timed per layer on the 7B, 27B and 7B-stack shapes): two token
+// tiles of the decode kernel (M > 8) double its MMAs, where the tcgen05 kernel's
+// N = 16 MMA costs the same; at M <= 8, plain layers of 2049..4608 rows.
+bool prefer_skinny_tc(int64_t M, int64_t rows, bool gated) {
+    if (M > 8) return true;
+    return !gated && rows > 2048 && rows <= 4608;
+}
+
 int gshift_of(int32_t group_size) {
     return group_size == 32 ? 5 : group_size == 64 ? 6 : group_size == 256 ? 8 : 7;
 }
@@ -237,7 +246,9 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     // skinny candidates: the decode kernel (M <= 16, any group size), then the
     // tcgen05 skinny kernel (M <= 32, not 64-wide groups)
     tl::GemvPlan gp{};
-    if (impl == kImplAuto && M <= tl::kGemvMaxM && !g32)
+    // the tcgen05 skinny kernel takes groups 0 / 128 / 256 and no zero-block map
+    const bool tc_can = !narrow && mask == nullptr;
+    if (impl == kImplAuto && M <= tl::kGemvMaxM && !g32 && !(tc_can && prefer_skinny_tc(M, N, false)))
         gp = tl::plan_gemv(M, N, K, d->sm_count, false, group, force_sk);
     tl::SkinnyTcPlan tp{};
     tl::SkinnyPlan mp{};
@@ -343,8 +354,9 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     const bool group = group_size != 0;
     const int gshift = gshift_of(group_size);
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
+    const bool tc_can = group_size != 64 && group_size != 32 && mask == nullptr;
     if (M <= skinny_max_m() && M <= tl::kGemvMaxM && skinny_impl() == kImplAuto &&
-        group_size != 32) {
+        group_size != 32 && !(tc_can && prefer_skinny_tc(M, 2 * N, true))) {
         tl::GemvPlan gp = tl::plan_gemv(M, 2 * N, K, d->sm_count, true, group_size != 0, force_sk);
         if (gp.ok) {
             tl::GemvArgs a{};
@@ -366,7 +378,7 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
             return from_cuda(tl::launch_gemv_silu(a, bf, group, gp, st, pdl_enabled()));
         }
     }
-    if (M <= skinny_max_m() && group_size != 64 && group_size != 32 && mask == nullptr) {
+    if (M <= skinny_max_m() && tc_can) {
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tl::SkinnyTcPlan tp = tl::plan_skinny_tc(M, 2 * N, K, d->sm_count, force_sk, per_sm);
         if (tp.ok) {

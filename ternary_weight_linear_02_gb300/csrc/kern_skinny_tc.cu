@@ -15,12 +15,15 @@ SkinnyTcPlan plan_skinny_tc(int64_t M, int64_t N, int64_t K, int sm_count, int f
     const int units = (int)((K + 127) / 128);
     // K is split (a thread-block cluster per row block) until the CTAs fill the
     // ctas_per_sm resident slots of every SM -- but never beyond them: a second,
-    // partial wave costs a whole CTA's latency
+    // partial wave costs a whole CTA's latency.  Clusters of 5 or 7 CTAs pack
+    // poorly into the GPCs (measured: 40 row blocks x 7 ran 1.6x slower than x 6),
+    // so those sizes step down to 4 and 6.
     const int64_t target = (int64_t)sm_count * (ctas_per_sm > 0 ? ctas_per_sm : 2);
     int sk = force_sk > 0 ? force_sk : (int)(target / p.row_tiles);
     if (sk < 1) sk = 1;
     if (sk > 8) sk = 8;
     if (sk > units) sk = units;
+    if (force_sk <= 0 && (sk == 5 || sk == 7)) --sk;
     const int upc = (units + sk - 1) / sk;  // units per CTA
     p.kc = upc * 128;
     p.sk = (int)((K + p.kc - 1) / p.kc);

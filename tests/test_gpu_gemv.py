@@ -1,11 +1,15 @@
-"""The decode kernel (gemv.cuh, M <= 16 tokens) against the oracle.
+"""Decode shapes (M <= 16 tokens, path "skinny") against the oracle.
 
-Covers both token-tile widths (M <= 8: one 8-token MMA tile, 9..16: two), every
-scale mode (per channel, 64-, 128- and 256-wide groups), K ranges that end
-inside a 256-k stage or hold fewer than one column per warp, ragged row
-counts, split K over 1..8 cluster CTAs, every output dtype (fp32 for each
-mode and token-tile width: the relative-L2 <= 1e-4 check of the accumulation),
-and the SiLU-gated gate/up variant.
+The automatic dispatch serves them with the register-fed decode kernel
+(gemv.cuh) or, for M > 8 and for plain layers of 2049..4608 rows, with the
+tcgen05 skinny kernel; 64-wide groups always run on the decode kernel, so its
+two-token-tile form (M = 9..16) is covered by the group-64 cases here and by
+the masked calls of test_gpu_mask.py.  Covers every scale mode (per channel,
+64-, 128- and 256-wide groups), K ranges that end inside a 256-k stage or hold
+fewer than one column per warp, ragged row counts, split K over 1..8 cluster
+CTAs, every output dtype (fp32 for each mode and token-tile width: the
+relative-L2 <= 1e-4 check of the accumulation), and the SiLU-gated gate/up
+variant.
 """
 import numpy as np
 import pytest

@@ -33,9 +33,11 @@ def _built():
     tl.load().ternary_test_set_wait_limit(0, 0)
 
 
-@pytest.mark.parametrize("M,N,K,gs", [(4, 4096, 4096, 0),    # split K: cluster barriers
+# shapes the decode kernel serves (64-wide groups and the 11008-row layer at
+# M = 1 stay on it; the dispatch sends other M > 8 calls to the tcgen05 kernel)
+@pytest.mark.parametrize("M,N,K,gs", [(4, 4096, 4096, 64),   # split K: cluster barriers
                                       (1, 11008, 4096, 128),  # no split K, group scales
-                                      (16, 300, 18944, 0)])   # two token tiles, split K
+                                      (16, 300, 18944, 64)])  # two token tiles, split K
 def test_wait_gives_up_then_recovers(M, N, K, gs):
     lib = tl.load()
     x, p, s = synth.layer(M, N, K, torch.bfloat16, gs, 0.005, 0.05, ("giveup", M, N, K), DEV)

@@ -57,6 +57,18 @@ CASES = [
 ]
 
 
+def same_kernel(M, N, gs, gated=False):
+    """Whether the unmasked call runs on the kernel the masked call runs on: the
+    automatic path sends some decode shapes (M > 8, or plain layers of
+    2049..4608 rows) to the tcgen05 skinny kernel, which reads no map, while
+    masked decode shapes run on the decode kernel."""
+    if M > 16 or gs == 64:
+        return True
+    if gated:
+        return M <= 8
+    return M <= 8 and not (2048 < N <= 4608)
+
+
 @pytest.mark.parametrize("M,N,K,xdt,gs", CASES)
 def test_masked_linear_equals_unmasked(M, N, K, xdt, gs):
     x, p, s = sparse_inputs(M, N, K, xdt, gs, 1)
@@ -65,7 +77,10 @@ def test_masked_linear_equals_unmasked(M, N, K, xdt, gs):
     skip = tl.linear(x, p, s, gs, out_dtype=torch.float32, mask=mask)
     torch.cuda.synchronize()
     assert int(zero.item()) > 0
-    assert torch.equal(dense, skip)
+    if same_kernel(M, N, gs):
+        assert torch.equal(dense, skip)
+    else:
+        check(dense, oracle_ref(x, p, s, gs), x, s, what=f"unmasked {M}x{N}x{K}")
     if N * K > 2048 * 2048:
         rows = np.unique(np.concatenate([np.arange(0, N, max(1, N // 83)), [N - 1]]))
         check(skip[:, rows], oracle_ref(x, p, s, gs, rows=rows), x, s, rows=rows,
@@ -100,6 +115,6 @@ def test_masked_silu_mul_equals_unmasked(M, N, K, gs):
     dense = tl.linear_silu_mul(x, p, s, gs, out_dtype=torch.float32)
     skip = tl.linear_silu_mul(x, p, s, gs, out_dtype=torch.float32, mask=mask)
     torch.cuda.synchronize()
-    assert torch.equal(dense, skip)
+    assert same_kernel(M, N, gs, gated=True) and torch.equal(dense, skip)
     h_ref, g_ref, u_ref = silu_refs(x, p, s, gs)
     check_silu(skip, h_ref, g_ref, u_ref, x, s, what=f"masked silu {M}x{N}x{K}")
