@@ -247,8 +247,8 @@ def per_m_entry(cfg, M, ms, pk, calls):
 
 def kernel_of(M):
     """The kernel family the automatic dispatch runs at M (K % 64 == 0)."""
-    if M <= 16:
-        return "decode kernel (warp MMAs, TMA-staged weights)"
+    if M <= 8:
+        return "decode kernel (warp MMAs, TMA-staged weights) and tcgen05 skinny kernel, per layer"
     if M <= 32:
         return "tcgen05 skinny kernel"
     return "tcgen05 tile kernel"
