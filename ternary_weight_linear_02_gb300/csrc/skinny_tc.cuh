@@ -28,17 +28,27 @@
 //    of codes per 64 k from the staged row (conflict-free thanks to the
 //    swizzle), decode every 2-bit code into 2*t in {+-2, +-0} (exact in fp16
 //    and bf16) with one shift + one AND per register (tl::pair2: codes j and
-//    j+8 of a 16-code word share one f16x2/bf16x2 register) and store each
-//    128-k unit into a TMEM A stage with tcgen05.st.  Set s decodes units
-//    u = s mod 2.  Decoders never wait for x.
+//    j+8 of a 16-code word share one f16x2/bf16x2 register) and store it
+//    into a TMEM A stage with tcgen05.st.  Channel scales: one A stage per
+//    64-k chunk h, decoded by set h mod 2.  Group scales: one A stage per 128-k
+//    unit u (a scale group), decoded by set u mod 2.  Decoders never wait for x.
 //  * Warp 9: permutes each 16-k block of every staged x row in place so that
 //    MMA k-slot (2j, 2j+1) holds x[j], x[j+8] -- the order in which pair2
 //    packs the weights -- then hands the stage to the MMA.
-//  * Warps 10-11 (MMA issuers): issuer s runs the tcgen05.mma (kind::f16,
-//    M = 128 rows, N = NT tokens, A from TMEM, B from shared memory) of units
-//    u = s mod 2 into its own fp32 TMEM accumulator.  One thread can issue a
-//    small-N MMA only every few dozen cycles, hence two issuers.
-//  * Scales.  Channel: the two issuers' accumulators are summed, reduced over
+//  * Warps 10.. (NI MMA issuers): issuer i runs the tcgen05.mma (kind::f16,
+//    M = 128 rows, N = NT tokens, A from TMEM, B from shared memory) of chunks
+//    h = i mod NI (channel scales) or units u = i mod 2 (group scales) into its
+//    own fp32 TMEM accumulator.  One warp issues a small-N MMA only every
+//    ~120-260 cycles whatever N is, and issuers in different warps proceed in
+//    parallel (measured on GB300), so issue is spread over NI warps: three at
+//    M <= 16, two where the accumulators take more TMEM.
+//  * Stage ownership.  The A-stage count NA is a multiple of 2 and of NI, so an
+//    A stage is always filled by the same decoder set and drained by the same
+//    issuer: each full/empty mbarrier pair then has one waiter that takes its
+//    phases in order.  (With an odd count, consecutive uses of a stage alternate
+//    between waiters, and a waiter one phase ahead can pass a parity wait on
+//    the phase before -- a parity wait cannot tell the two apart.)
+//  * Scales.  Channel: the issuers' accumulators are summed, reduced over
 //    the split K, then multiplied by 0.5*s[n] (the 2 of the +-2 decode).
 //    Group: each 128-k unit lands in its issuer's accumulator slot; the decoder
 //    set that owns the unit reads it back (tcgen05.ld) and folds
@@ -72,15 +82,20 @@ constexpr int kSmemFloor = 96 * 1024;  // keeps residency at <= two CTAs per SM
 
 // warp roles
 // warps 0-7: two decoder sets (set = warp / 4, lane quarter = warp % 4)
-constexpr int kWarpProd = 8, kWarpPerm = 9, kWarpMma0 = 10, kWarpMma1 = 11;
-constexpr int kThreads = 384;
+constexpr int kWarpProd = 8, kWarpPerm = 9, kWarpMma0 = 10;
 constexpr int kUnitsPerW = 4;        // 128-k units per weight stage (512 k)
 constexpr int kWStage = 128 * 128;   // packed bytes per weight stage (128 rows x 128 B)
 
 template <int NT, bool GROUP>
 struct SkCfg {
-    // two MMA issuers, one TMEM accumulator slot each (group mode: units alternate)
-    static constexpr int NA = (int)((kTmemCols - 2u * NT) / 64);  // A stages (128 k)
+    // Channel scales: A stages of one 64-k chunk (32 TMEM columns) and NI issuers,
+    // each with its own accumulator.  Group scales: A stages of one 128-k unit and
+    // two issuers whose accumulator slots hold one unit at a time.
+    static constexpr bool CH = !GROUP;
+    static constexpr int NI = (CH && NT == 16) ? 3 : 2;     // MMA issuer warps
+    static constexpr int ACOLS = CH ? 32 : 64;              // TMEM columns per A stage
+    static constexpr int NA = CH ? 6 : 2;                   // A stages
+    static constexpr int THREADS = (kWarpMma0 + NI) * 32;
     static constexpr int XB = NT == 16 ? 8 : 4;       // 64-k x boxes per x stage
     static constexpr int UPX = XB / 2;                // units per x stage
     static constexpr int XBOX = NT * 128;             // one box: NT rows x 128 B
@@ -92,10 +107,11 @@ struct SkCfg {
     // split-K receive rows: sk * ceil(128/sk) <= 135, or (gated) sk * 2 * ceil(64/sk) <= 140
     static constexpr int RECV_BYTES = (128 + 16) * NT * 4;
     static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
-    static constexpr int NBARS = 3 * XS + 2 * WS + 2 * NA + 7;
+    static constexpr int NBARS = 3 * XS + 2 * WS + 2 * NA + 3 * NI + 1;
     static constexpr int USED = BAR_OFF + NBARS * 8 + 16;
     static constexpr int SMEM = (USED + 1024 > kSmemFloor) ? USED + 1024 : kSmemFloor;
-    static_assert(NA >= 2, "TMEM budget");
+    static_assert(NA * ACOLS + NI * NT <= (int)kTmemCols, "TMEM budget");
+    static_assert(NA % 2 == 0 && NA % NI == 0, "each A stage has one decoder set and one issuer");
     static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
@@ -193,7 +209,7 @@ __device__ __forceinline__ void decode_chunk(const uint4 &c, uint32_t (&r)[32]) 
 }
 
 template <int NT, bool BF, bool GROUP, int OUT, bool SILU>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(SkCfg<NT, GROUP>::THREADS, 2)
     skinny_tc_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmw,
                      SkinnyTcArgs a) {
     using C = SkCfg<NT, GROUP>;
@@ -207,8 +223,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint64_t *tfull = bars, *bfull = bars + C::XS, *xempty = bars + 2 * C::XS;
     uint64_t *wfull = bars + 3 * C::XS, *wempty = wfull + C::WS;
     uint64_t *afull = wempty + C::WS, *aempty = afull + C::NA;
-    uint64_t *dfull = aempty + C::NA, *dempty = dfull + 2, *mdone = dempty + 2;
-    uint64_t *rbar = mdone + 2;
+    uint64_t *dfull = aempty + C::NA, *dempty = dfull + C::NI, *mdone = dempty + C::NI;
+    uint64_t *rbar = mdone + C::NI;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -236,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int i = 0; i < C::XS; ++i) {
             mbar_init(&tfull[i], 1);
             mbar_init(&bfull[i], 1);
-            mbar_init(&xempty[i], 2);  // one commit per MMA issuer
+            mbar_init(&xempty[i], C::NI);  // one commit per MMA issuer
         }
         for (int i = 0; i < C::WS; ++i) {
             mbar_init(&wfull[i], 1);
@@ -246,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             mbar_init(&afull[i], 4);
             mbar_init(&aempty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < C::NI; ++i) {
             mbar_init(&dfull[i], 1);
             mbar_init(&dempty[i], 4);
             mbar_init(&mdone[i], 1);
@@ -262,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc::fence_after_sync();
     if (sk > 1) cluster_arrive_aligned();  // this CTA's barriers are initialised
     const uint32_t tmem = *tmem_slot;
-    const uint32_t dbase = tmem + (uint32_t)(C::NA * 64);
+    const uint32_t dbase = tmem + (uint32_t)(C::NA * C::ACOLS);
     // dependents may start once every CTA of this grid holds its TMEM
     if (!(a.flags & (kSkinnyTriggerLate | kSkinnyTriggerNever))) pdl_launch_dependents();
 
@@ -373,9 +389,56 @@ __global__ void __launch_bounds__(kThreads, 2)
             __syncwarp();
             if (lane == 0) mbar_arrive(&bfull[s]);
         }
-    } else if (warp == kWarpMma0 || warp == kWarpMma1) {
-        // ------------------------------------------------ MMA issuers: issuer i takes units u = i mod 2
-        const int iss = warp == kWarpMma0 ? 0 : 1;
+    } else if (warp >= kWarpMma0 && C::CH) {
+        // ------------------------------------------------ MMA issuers, channel scales:
+        // issuer iss takes chunks h = iss mod NI (A stages iss, iss + NI, ...) and
+        // accumulates all of them into its own slot
+        const int iss = warp - kWarpMma0;
+        constexpr uint32_t idesc = tc::idesc_f16(NT, BF);
+        const uint32_t d = dbase + (uint32_t)(iss * NT);
+        bool ok = true, first = true;
+        for (int i = 0; i < nxs && ok; ++i) {
+            const int s = i % C::XS;
+            if (!warp_wait(&bfull[s], (i / C::XS) & 1, lane)) {
+                ok = false;
+                break;
+            }
+            const uint64_t xdesc = tc::desc_sw128(xring + (size_t)s * C::XSTAGE);
+            const int hb = i * C::XB, he = min(nch, hb + C::XB);
+            for (int h = hb + (iss - hb % C::NI + C::NI) % C::NI; h < he; h += C::NI) {
+                const int st = h % C::NA;
+                if (!warp_wait(&afull[st], (h / C::NA) & 1, lane)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    tc::fence_after_sync();
+                    const uint32_t acol = tmem + (uint32_t)(st * C::ACOLS);
+                    const uint64_t b0 = xdesc + (uint64_t)(((h - hb) * C::XBOX) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_ts(d, acol + kk * 8, b0 + (uint64_t)(kk * 2), idesc,
+                                   (first && kk == 0) ? 0u : 1u);  // the first MMA overwrites the slot
+                    tc::commit(&aempty[st]);
+                }
+                first = false;
+                __syncwarp();
+            }
+            if (lane == 0) tc::commit(&xempty[s]);
+            __syncwarp();
+        }
+        if (lane == 0) {
+            if (!ok) give_up();
+            tc::commit(&dfull[iss]);
+            // drain: every MMA of this issuer has completed before TMEM is released
+            tc::commit(&mdone[iss]);
+        }
+        __syncwarp();
+        if (!warp_wait(&mdone[iss], 0, lane) && lane == 0) give_up();
+    } else if (warp >= kWarpMma0) {
+        // ------------------------------------------------ MMA issuers, group scales:
+        // issuer iss takes units u = iss mod 2, one unit per accumulator fill
+        const int iss = warp - kWarpMma0;
         constexpr uint32_t idesc = tc::idesc_f16(NT, BF);
         const uint32_t d = dbase + (uint32_t)(iss * NT);
         bool ok = true;
@@ -390,15 +453,15 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int u = ub + ((ub & 1) != iss ? 1 : 0); u < ue; u += 2) {
                 const int st = u % C::NA;
                 if (!warp_wait(&afull[st], (u / C::NA) & 1, lane) ||
-                    (GROUP && u >= 2 && !warp_wait(&dempty[iss], ((u >> 1) - 1) & 1, lane))) {
+                    (u >= 2 && !warp_wait(&dempty[iss], ((u >> 1) - 1) & 1, lane))) {
                     ok = false;
                     break;
                 }
                 if (lane == 0) {
                     tc::fence_after_sync();
-                    const uint32_t acol = tmem + (uint32_t)(st * 64);
+                    const uint32_t acol = tmem + (uint32_t)(st * C::ACOLS);
                     const uint64_t b0 = xdesc + (uint64_t)((2 * (u - ub) * C::XBOX) >> 4);
-                    const bool fresh = GROUP || u == iss;  // first MMA overwrites the slot
+                    constexpr bool fresh = true;  // every unit overwrites the slot
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         tc::mma_ts(d, acol + kk * 8, b0 + (uint64_t)(kk * 2), idesc,
@@ -410,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                             tc::mma_ts(d, acol + 32 + kk * 8, b1 + (uint64_t)(kk * 2), idesc, 1u);
                     }
                     tc::commit(&aempty[st]);
-                    if (GROUP) tc::commit(&dfull[iss]);
+                    tc::commit(&dfull[iss]);
                 }
                 __syncwarp();
             }
@@ -419,7 +482,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (lane == 0) {
             if (!ok) give_up();
-            if (!GROUP) tc::commit(&dfull[iss]);
             // drain: every MMA of this issuer has completed before TMEM is released
             tc::commit(&mdone[iss]);
         }
@@ -427,8 +489,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (!warp_wait(&mdone[iss], 0, lane) && lane == 0) give_up();
     } else {
         // ------------------------------------------------ decoders (thread = weight row)
-        // Set s = warp / 4 decodes units u = s mod 2 (consumed by MMA issuer s, whose
-        // accumulator slot is s); warp % 4 selects the TMEM lane quarter.
+        // Set s = warp / 4 decodes the chunks (channel scales) or units (group
+        // scales) of parity s; warp % 4 selects the TMEM lane quarter.
         const int set = warp >> 2, q = warp & 3;
         const int row = q * 32 + lane;
         const int n = SILU ? (row < 64 ? j0 + row : a.nh + j0 + row - 64) : n0 + row;
@@ -444,95 +506,139 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int j = 0; j < NT; ++j) acc[j] = 0.f;
 
         bool ok = true;
-        // fold unit v's accumulator slot (v mod 2 = set) into acc with the group scale sv
-        auto fold = [&](int v, float sv) {
-            const int slot = v & 1;
-            ok = ok && warp_wait(&dfull[slot], (v >> 1) & 1, lane);
-            if (!ok) return;
-            tc::fence_after_sync();
-#pragma unroll
-            for (int h = 0; h < NT / 16; ++h) {  // 16 columns at a time keeps registers low
-                uint32_t dv[16];
-                ld_32x32b_x16(tlane + (uint32_t)(C::NA * 64 + slot * NT + 16 * h), dv);
-                tc::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j) acc[16 * h + j] = fmaf(sv, __uint_as_float(dv[j]), acc[16 * h + j]);
+        if constexpr (C::CH) {
+            // chunk h (64 k) -> A stage h mod NA, multiplied by issuer h mod NI.
+            // Software pipeline: the next chunk is decoded while this one's TMEM
+            // store is in flight (tcgen05.wait::st comes after it).
+            uint4 cw = make_uint4(0, 0, 0, 0);
+            // codes of chunk h into cw; releases a weight stage after this set's
+            // last chunk in it (the final stage is never refilled)
+            auto load_chunk = [&](int h) -> bool {
+                const int w = h >> 3, ws = w % C::WS, uw = h & 7;
+                if (uw < 2 && !warp_wait(&wfull[ws], (w / C::WS) & 1, lane)) return false;
+                cw = *reinterpret_cast<const uint4 *>(wrow + (size_t)ws * kWStage + ((uw ^ sw) << 4));
+                if (uw >= 6 && w + 1 < nws) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&wempty[ws]);  // codes are in registers
+                }
+                return true;
+            };
+            uint32_t r[32];
+            if (set < nch) {
+                ok = load_chunk(set);
+                decode_chunk(cw, r);
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&dempty[slot]);
-        };
-
-        // Software pipeline: the next unit's first chunk is decoded while this
-        // unit's TMEM stores are in flight (tcgen05.wait::st comes after it).
-        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
-        float su = 0.f, s_prev = 0.f;
-        // codes (and group scale) of unit v into c0/c1/su; releases a weight stage
-        // after this set's last unit in it (the final stage is never refilled)
-        auto load_unit = [&](int v) -> bool {
-            const int w = v / kUnitsPerW, ws = w % C::WS, uw = v % kUnitsPerW;
-            if (uw < 2 && !warp_wait(&wfull[ws], (w / C::WS) & 1, lane)) return false;
-            const uint8_t *stage = wrow + (size_t)ws * kWStage;
-            c0 = *reinterpret_cast<const uint4 *>(stage + (((2 * uw) ^ sw) << 4));
-            c1 = (2 * v + 1 < nch) ? *reinterpret_cast<const uint4 *>(stage + (((2 * uw + 1) ^ sw) << 4))
-                                   : make_uint4(0, 0, 0, 0);
-            su = (GROUP && rowok) ? 0.5f * h2f(srow[(g0 + v) >> gsh]) : 0.f;
-            if (uw >= 2 && w + 1 < nws) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&wempty[ws]);  // codes are in registers
-            }
-            return true;
-        };
-        uint32_t r[32];
-        if (set < nun) {
-            ok = load_unit(set);
-            decode_chunk(c0, r);
-        }
-        for (int u = set; u < nun && ok; u += 2) {
-            const int st = u % C::NA;
-            const bool two = 2 * u + 1 < nch;
-            const float su_u = su;
-            const uint4 c1_u = c1;
-            if (u >= C::NA && !warp_wait(&aempty[st], ((u / C::NA) - 1) & 1, lane)) {
-                ok = false;
-                break;
-            }
-            tc::st_32x32b_x32(tlane + (uint32_t)(st * 64), r);
-            if (two) {
-                decode_chunk(c1_u, r);
-                tc::st_32x32b_x32(tlane + (uint32_t)(st * 64 + 32), r);
-            }
-            if (u + 2 < nun) {
-                if (!load_unit(u + 2)) {
+            for (int h = set; h < nch && ok; h += 2) {
+                const int st = h % C::NA;
+                if (h >= C::NA && !warp_wait(&aempty[st], ((h / C::NA) - 1) & 1, lane)) {
                     ok = false;
                     break;
                 }
-                decode_chunk(c0, r);  // overlaps the stores above
+                tc::st_32x32b_x32(tlane + (uint32_t)(st * C::ACOLS), r);
+                if (h + 2 < nch) {
+                    if (!load_chunk(h + 2)) {
+                        ok = false;
+                        break;
+                    }
+                    decode_chunk(cw, r);  // overlaps the store above
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[st]);
             }
-            tc::wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[st]);
-            if (GROUP && u >= 2) {
-                fold(u - 2, s_prev);
-                if (!ok) break;
-            }
-            s_prev = su_u;
-        }
-        if (GROUP && ok && set < nun) fold(set + ((nun - 1 - set) / 2) * 2, s_prev);
-        if (!GROUP && ok && set == 0) {
-            // sum of the two issuers' accumulators
-            for (int i = 0; i < 2 && i < nun && ok; ++i) {
-                ok = warp_wait(&dfull[i], 0, lane);
-                if (!ok) break;
-                tc::fence_after_sync();
-                uint32_t dv[NT];
-                ld_d<NT>(tlane + (uint32_t)(C::NA * 64 + i * NT), dv);
-                tc::wait_ld();
+            if (ok && set == 0) {
+                // sum of the accumulators of the issuers that ran (issuer j's first chunk is j)
+                const int nvalid = nch < C::NI ? nch : C::NI;
+                for (int j = 0; j < nvalid && ok; ++j) {
+                    ok = warp_wait(&dfull[j], 0, lane);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    uint32_t dv[NT];
+                    ld_d<NT>(tlane + (uint32_t)(C::NA * C::ACOLS + j * NT), dv);
+                    tc::wait_ld();
 #pragma unroll
-                for (int j = 0; j < NT; ++j)
-                    acc[j] = (i == 0) ? __uint_as_float(dv[j]) : acc[j] + __uint_as_float(dv[j]);
+                    for (int m = 0; m < NT; ++m)
+                        acc[m] = (j == 0) ? __uint_as_float(dv[m]) : acc[m] + __uint_as_float(dv[m]);
+                }
             }
+        } else {
+            // fold unit v's accumulator slot (v mod 2 = set) into acc with the group scale sv
+            auto fold = [&](int v, float sv) {
+                const int slot = v & 1;
+                ok = ok && warp_wait(&dfull[slot], (v >> 1) & 1, lane);
+                if (!ok) return;
+                tc::fence_after_sync();
+#pragma unroll
+                for (int h = 0; h < NT / 16; ++h) {  // 16 columns at a time keeps registers low
+                    uint32_t dv[16];
+                    ld_32x32b_x16(tlane + (uint32_t)(C::NA * C::ACOLS + slot * NT + 16 * h), dv);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) acc[16 * h + j] = fmaf(sv, __uint_as_float(dv[j]), acc[16 * h + j]);
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dempty[slot]);
+            };
+
+            // Software pipeline: the next unit's first chunk is decoded while this
+            // unit's TMEM stores are in flight (tcgen05.wait::st comes after it).
+            uint4 c0 = make_uint4(0, 0, 0, 0), c1 = make_uint4(0, 0, 0, 0);
+            float su = 0.f, s_prev = 0.f;
+            // codes (and group scale) of unit v into c0/c1/su; releases a weight stage
+            // after this set's last unit in it (the final stage is never refilled)
+            auto load_unit = [&](int v) -> bool {
+                const int w = v / kUnitsPerW, ws = w % C::WS, uw = v % kUnitsPerW;
+                if (uw < 2 && !warp_wait(&wfull[ws], (w / C::WS) & 1, lane)) return false;
+                const uint8_t *stage = wrow + (size_t)ws * kWStage;
+                c0 = *reinterpret_cast<const uint4 *>(stage + (((2 * uw) ^ sw) << 4));
+                c1 = (2 * v + 1 < nch) ? *reinterpret_cast<const uint4 *>(stage + (((2 * uw + 1) ^ sw) << 4))
+                                       : make_uint4(0, 0, 0, 0);
+                su = (GROUP && rowok) ? 0.5f * h2f(srow[(g0 + v) >> gsh]) : 0.f;
+                if (uw >= 2 && w + 1 < nws) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&wempty[ws]);  // codes are in registers
+                }
+                return true;
+            };
+            uint32_t r[32];
+            if (set < nun) {
+                ok = load_unit(set);
+                decode_chunk(c0, r);
+            }
+            for (int u = set; u < nun && ok; u += 2) {
+                const int st = u % C::NA;
+                const bool two = 2 * u + 1 < nch;
+                const float su_u = su;
+                const uint4 c1_u = c1;
+                if (u >= C::NA && !warp_wait(&aempty[st], ((u / C::NA) - 1) & 1, lane)) {
+                    ok = false;
+                    break;
+                }
+                tc::st_32x32b_x32(tlane + (uint32_t)(st * C::ACOLS), r);
+                if (two) {
+                    decode_chunk(c1_u, r);
+                    tc::st_32x32b_x32(tlane + (uint32_t)(st * C::ACOLS + 32), r);
+                }
+                if (u + 2 < nun) {
+                    if (!load_unit(u + 2)) {
+                        ok = false;
+                        break;
+                    }
+                    decode_chunk(c0, r);  // overlaps the stores above
+                }
+                tc::wait_st();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&afull[st]);
+                if (GROUP && u >= 2) {
+                    fold(u - 2, s_prev);
+                    if (!ok) break;
+                }
+                s_prev = su_u;
+            }
+            if (GROUP && ok && set < nun) fold(set + ((nun - 1 - set) / 2) * 2, s_prev);
         }
         if (!ok) give_up();
         if (GROUP) {
@@ -705,7 +811,7 @@ cudaError_t launch_one(const SkinnyTcArgs &a, const SkinnyTcPlan &p, cudaStream_
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.row_tiles, (unsigned)p.sk, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
