@@ -66,9 +66,11 @@ int skinny_launch_flags(uint32_t api_flags) {
     return base | ((api_flags & TL_FLAG_STATIC_WEIGHTS) ? tl::kSkinnyStaticWeights : 0);
 }
 
-// Skinny-path kernel choice.  M <= 16: the decode kernel of gemv.cuh (register-fed
-// warp MMAs, TMA-staged weights, x fragments held in registers per 64-k column).
-// 17 <= M <= 32: the tcgen05 kernel (decoded weights in TMEM, 128-row tiles).
+// Skinny-path kernel choice (prefer_skinny_tc below).  The decode kernel of
+// gemv.cuh (register-fed warp MMAs, TMA-staged weights, x fragments held in
+// registers per 64-k column) serves M <= 8 except plain layers of 2049..4608
+// rows, 64-wide groups and zero-block maps at M <= 16; the tcgen05 kernel
+// (decoded weights in TMEM, 128-row tiles) serves the rest up to M = 32.
 //   TERNARY_SKINNY_IMPL=tc | mma   force the tcgen05 kernel, or the older warp-MMA
 //                                  kernel of kern_skinny.cu, for every M <= 32
 enum { kImplAuto = 0, kImplMma = 1, kImplTc = 2 };
