@@ -197,12 +197,13 @@ tl_status ternary_block_mask(const uint8_t *packed, int64_t N, int64_t K, uint32
  * ternary_linear_silu_mul (same arguments, TL_PATH_AUTO) that read the zero-block
  * map `mask` of the same packed matrix (for the gated call: of all 2N stacked
  * rows) and neither load nor multiply blocks whose bit is 0 (a zero bit is the
- * caller's promise that the block's weights are zero).  Decode shapes (M <= 16)
- * run on the decode kernel, the rest on the tile kernel.  With the map that
- * ternary_block_mask built, the result equals the unmasked call's bit for bit
- * whenever the unmasked call runs on the same kernel -- always for M > 16 and
- * for 64-wide groups; the decode shapes that the automatic path sends to the
- * tcgen05 skinny kernel (which reads no map) agree within the stated tolerance.
+ * caller's promise that the block's weights are zero).  With per-channel scales
+ * and with 64-wide groups the masked call runs on the kernel the unmasked call
+ * runs on; with 128- and 256-wide groups the tcgen05 skinny kernel reads no map,
+ * so masked calls at M <= 32 run on the decode kernel (M <= 16) or the tile
+ * kernel.  With the map that ternary_block_mask built, the result equals the
+ * unmasked call's bit for bit whenever both run on the same kernel (up to the
+ * sign of an exact zero), and agrees within the stated tolerance otherwise.
  * mask: device, 4-byte aligned, NULL only when nothing is computed.
  */
 tl_status ternary_linear_masked(const void *x, int32_t x_dtype, const uint8_t *packed,
@@ -218,9 +219,10 @@ tl_status ternary_linear_silu_mul_masked(const void *x, int32_t x_dtype, const u
 /* Kernels by M (TL_PATH_AUTO, K % 64 == 0): M <= 16 -> the decode kernel
  * (register-fed warp MMAs, TMA-staged weights) or, for 9 <= M and for plain
  * layers of 2049..4608 rows at M <= 8, the tcgen05 skinny kernel (groups 0 /
- * 128 / 256, no zero-block map: whichever was measured faster on the 7B and 27B
- * shapes); 17 <= M <= 32 -> the tcgen05 skinny kernel (64-wide groups: tile
- * kernel); larger M -> the tcgen05 tile kernel.  32-wide groups run on the tile
+ * 128 / 256; a zero-block map only with per-channel scales: whichever was
+ * measured faster on the 7B and 27B shapes); 17 <= M <= 32 -> the tcgen05
+ * skinny kernel (64-wide groups: tile kernel); larger M -> the tcgen05 tile
+ * kernel.  32-wide groups run on the tile
  * kernel at every M; K % 64 != 0 runs on the generic kernel at every M, which
  * reads no zero-block map (the masked calls then equal the unmasked ones
  * trivially). */

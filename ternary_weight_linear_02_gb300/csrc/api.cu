@@ -248,14 +248,15 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
     // skinny candidates: the decode kernel (M <= 16, any group size), then the
     // tcgen05 skinny kernel (M <= 32, not 64-wide groups)
     tl::GemvPlan gp{};
-    // the tcgen05 skinny kernel takes groups 0 / 128 / 256 and no zero-block map
-    const bool tc_can = !narrow && mask == nullptr;
+    // the tcgen05 skinny kernel takes groups 0 / 128 / 256, and a zero-block map
+    // with per-channel scales
+    const bool tc_can = !narrow && (mask == nullptr || !group);
     if (impl == kImplAuto && M <= tl::kGemvMaxM && !g32 && !(tc_can && prefer_skinny_tc(M, N, false)))
         gp = tl::plan_gemv(M, N, K, d->sm_count, false, group, force_sk);
     tl::SkinnyTcPlan tp{};
     tl::SkinnyPlan mp{};
-    // the zero-block map is read by the decode kernel and the tile kernel only
-    if (!gp.ok && !narrow && impl != kImplMma && mask == nullptr) {
+    // the zero-block map is read by the decode, tile and (channel scales) tcgen05 skinny kernels
+    if (!gp.ok && tc_can && impl != kImplMma) {
         static const int per_sm = env_int("TERNARY_SKINNY_CTAS_PER_SM", 2);
         tp = tl::plan_skinny_tc(M, N, K, d->sm_count, force_sk, per_sm);
     }
@@ -299,6 +300,8 @@ tl_status run_linear(const void *x, int32_t x_dtype, const uint8_t *packed, cons
             a.gshift = gshift;
             a.flags = skinny_launch_flags(flags);
             a.status = d->status;
+            a.mask = mask;
+            a.mask_words = tl::mask_words(K);
             return from_cuda(tl::launch_skinny_tc(a, bf, group, out_dtype, tp, st, pdl_enabled()));
         }
         tl::SkinnyArgs a{};
@@ -356,7 +359,7 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
     const bool group = group_size != 0;
     const int gshift = gshift_of(group_size);
     static const int force_sk = env_int("TERNARY_SKINNY_SK", 0);
-    const bool tc_can = group_size != 64 && group_size != 32 && mask == nullptr;
+    const bool tc_can = group_size != 64 && group_size != 32 && (mask == nullptr || group_size == 0);
     if (M <= skinny_max_m() && M <= tl::kGemvMaxM && skinny_impl() == kImplAuto &&
         group_size != 32 && !(tc_can && prefer_skinny_tc(M, 2 * N, true))) {
         tl::GemvPlan gp = tl::plan_gemv(M, 2 * N, K, d->sm_count, true, group_size != 0, force_sk);
@@ -396,6 +399,8 @@ tl_status run_silu_mul(const void *x, int32_t x_dtype, const uint8_t *packed, co
             a.gshift = gshift;
             a.flags = skinny_launch_flags(flags);
             a.status = d->status;
+            a.mask = mask;
+            a.mask_words = tl::mask_words(K);
             return from_cuda(tl::launch_skinny_silu(a, bf, group, out_dtype, tp, st, pdl_enabled()));
         }
     }

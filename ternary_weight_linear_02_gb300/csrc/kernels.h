@@ -84,6 +84,8 @@ struct SkinnyTcArgs {
     int kc;                  // k per CTA (multiple of 128), set from the plan
     int flags;               // kSkinny* bits
     int *status;             // device status word (bounded-wait failures)
+    const uint32_t *mask;    // zero-block map (channel scales only; nullptr: every block is read)
+    int mask_words;          // map words per 128-row block
 };
 
 struct SkinnyTcPlan {

@@ -107,11 +107,12 @@ struct SkCfg {
     // split-K receive rows: sk * ceil(128/sk) <= 135, or (gated) sk * 2 * ceil(64/sk) <= 140
     static constexpr int RECV_BYTES = (128 + 16) * NT * 4;
     static constexpr int BAR_OFF = RECV_OFF + RECV_BYTES;
-    static constexpr int NBARS = 3 * XS + 2 * WS + 2 * NA + 3 * NI + 1;
+    static constexpr int NBARS = 3 * XS + 2 * WS + 2 * NA + 3 * NI + 2;
     static constexpr int USED = BAR_OFF + NBARS * 8 + 16;
     static constexpr int SMEM = (USED + 1024 > kSmemFloor) ? USED + 1024 : kSmemFloor;
     static_assert(NA * ACOLS + NI * NT <= (int)kTmemCols, "TMEM budget");
     static_assert(NA % 2 == 0 && NA % NI == 0, "each A stage has one decoder set and one issuer");
+    static_assert(!CH || NA * ACOLS + 64 <= (int)kTmemCols, "two 32-column stores zero the accumulators");
     static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(SkCfg<NT, GROUP>::THREADS, 2)
     uint64_t *wfull = bars + 3 * C::XS, *wempty = wfull + C::WS;
     uint64_t *afull = wempty + C::WS, *aempty = afull + C::NA;
     uint64_t *dfull = aempty + C::NA, *dempty = dfull + C::NI, *mdone = dempty + C::NI;
-    uint64_t *rbar = mdone + C::NI;
+    uint64_t *rbar = mdone + C::NI, *dzero = rbar + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::NBARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -269,6 +270,7 @@ __global__ void __launch_bounds__(SkCfg<NT, GROUP>::THREADS, 2)
         }
         // one arrival per (sender, row of this slice)
         mbar_init(rbar, (uint32_t)(SILU ? sk * 2 * plen : sk * slen));
+        mbar_init(dzero, 4);  // decoder set 0 has zeroed the accumulators (channel scales)
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -281,6 +283,29 @@ __global__ void __launch_bounds__(SkCfg<NT, GROUP>::THREADS, 2)
     const uint32_t dbase = tmem + (uint32_t)(C::NA * C::ACOLS);
     // dependents may start once every CTA of this grid holds its TMEM
     if (!(a.flags & (kSkinnyTriggerLate | kSkinnyTriggerNever))) pdl_launch_dependents();
+
+    // Zero-block map (a.mask, optional; channel scales only): bit kb of word
+    // [rb][kb / 32] is set when rows [128 rb, +128) x k [64 kb, +64) hold a
+    // non-zero weight.  A chunk whose blocks are zero for this CTA's rows is
+    // neither decoded nor multiplied; its codes are still staged (the weight
+    // ring keeps its order) and every chunk keeps its decoder set, issuer and A
+    // stage, so a masked call adds the same partial sums in the same order as
+    // an unmasked one.
+    auto rows_live = [&](int r0, int r1, int kb) -> bool {
+        if (r1 <= r0) return false;
+        for (int rb = r0 >> 7; rb <= (r1 - 1) >> 7; ++rb)
+            if ((__ldg(a.mask + (int64_t)rb * a.mask_words + (kb >> 5)) >> (kb & 31)) & 1u) return true;
+        return false;
+    };
+    auto chunk_live = [&](int h) -> bool {  // chunk h of this CTA's K range
+        if (!C::CH || a.mask == nullptr) return true;
+        const int kb = (k0 >> 6) + h;
+        if constexpr (SILU)
+            return rows_live(j0, min(j0 + 64, a.nh), kb) ||
+                   rows_live(a.nh + j0, min(a.nh + j0 + 64, 2 * a.nh), kb);
+        else
+            return rows_live(n0, min(n0 + 128, a.N), kb);
+    };
 
     auto give_up = [&]() {
         *abort_flag = 1;
@@ -391,41 +416,79 @@ __global__ void __launch_bounds__(SkCfg<NT, GROUP>::THREADS, 2)
         }
     } else if (warp >= kWarpMma0 && C::CH) {
         // ------------------------------------------------ MMA issuers, channel scales:
-        // issuer iss takes chunks h = iss mod NI (A stages iss, iss + NI, ...) and
-        // accumulates all of them into its own slot
+        // issuer iss takes chunks h = iss mod NI (A stages iss, iss + NI, ...) into its
+        // own slot: without a zero-block map every chunk, the first MMA overwriting
+        // the slot; with one the live chunks only, into a slot decoder set 0 zeroed
         const int iss = warp - kWarpMma0;
         constexpr uint32_t idesc = tc::idesc_f16(NT, BF);
         const uint32_t d = dbase + (uint32_t)(iss * NT);
-        bool ok = true, first = true;
-        for (int i = 0; i < nxs && ok; ++i) {
-            const int s = i % C::XS;
-            if (!warp_wait(&bfull[s], (i / C::XS) & 1, lane)) {
-                ok = false;
-                break;
-            }
-            const uint64_t xdesc = tc::desc_sw128(xring + (size_t)s * C::XSTAGE);
-            const int hb = i * C::XB, he = min(nch, hb + C::XB);
-            for (int h = hb + (iss - hb % C::NI + C::NI) % C::NI; h < he; h += C::NI) {
-                const int st = h % C::NA;
-                if (!warp_wait(&afull[st], (h / C::NA) & 1, lane)) {
+        bool ok = true;
+        if (a.mask == nullptr) {
+            bool first = true;
+            for (int i = 0; i < nxs && ok; ++i) {
+                const int s = i % C::XS;
+                if (!warp_wait(&bfull[s], (i / C::XS) & 1, lane)) {
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    tc::fence_after_sync();
-                    const uint32_t acol = tmem + (uint32_t)(st * C::ACOLS);
-                    const uint64_t b0 = xdesc + (uint64_t)(((h - hb) * C::XBOX) >> 4);
+                const uint64_t xdesc = tc::desc_sw128(xring + (size_t)s * C::XSTAGE);
+                const int hb = i * C::XB, he = min(nch, hb + C::XB);
+                for (int h = hb + (iss - hb % C::NI + C::NI) % C::NI; h < he; h += C::NI) {
+                    const int st = h % C::NA;
+                    if (!warp_wait(&afull[st], (h / C::NA) & 1, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tc::fence_after_sync();
+                        const uint32_t acol = tmem + (uint32_t)(st * C::ACOLS);
+                        const uint64_t b0 = xdesc + (uint64_t)(((h - hb) * C::XBOX) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        tc::mma_ts(d, acol + kk * 8, b0 + (uint64_t)(kk * 2), idesc,
-                                   (first && kk == 0) ? 0u : 1u);  // the first MMA overwrites the slot
-                    tc::commit(&aempty[st]);
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_ts(d, acol + kk * 8, b0 + (uint64_t)(kk * 2), idesc,
+                                       (first && kk == 0) ? 0u : 1u);  // the first MMA overwrites the slot
+                        tc::commit(&aempty[st]);
+                    }
+                    first = false;
+                    __syncwarp();
                 }
-                first = false;
+                if (lane == 0) tc::commit(&xempty[s]);
                 __syncwarp();
             }
-            if (lane == 0) tc::commit(&xempty[s]);
-            __syncwarp();
+        } else {
+            // zero-block map: live chunks only, accumulators zeroed by decoder set 0
+            ok = warp_wait(dzero, 0, lane);
+            uint32_t par = 0;  // bit st: uses of A stage st so far, mod 2 (its next afull phase)
+            for (int i = 0; i < nxs && ok; ++i) {
+                const int s = i % C::XS;
+                if (!warp_wait(&bfull[s], (i / C::XS) & 1, lane)) {
+                    ok = false;
+                    break;
+                }
+                const uint64_t xdesc = tc::desc_sw128(xring + (size_t)s * C::XSTAGE);
+                const int hb = i * C::XB, he = min(nch, hb + C::XB);
+                for (int h = hb + (iss - hb % C::NI + C::NI) % C::NI; h < he; h += C::NI) {
+                    if (!chunk_live(h)) continue;
+                    const int st = h % C::NA;
+                    if (!warp_wait(&afull[st], (par >> st) & 1u, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        tc::fence_after_sync();
+                        const uint32_t acol = tmem + (uint32_t)(st * C::ACOLS);
+                        const uint64_t b0 = xdesc + (uint64_t)(((h - hb) * C::XBOX) >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            tc::mma_ts(d, acol + kk * 8, b0 + (uint64_t)(kk * 2), idesc, 1u);
+                        tc::commit(&aempty[st]);
+                    }
+                    par ^= 1u << st;
+                    __syncwarp();
+                }
+                if (lane == 0) tc::commit(&xempty[s]);
+                __syncwarp();
+            }
         }
         if (lane == 0) {
             if (!ok) give_up();
@@ -507,50 +570,135 @@ __global__ void __launch_bounds__(SkCfg<NT, GROUP>::THREADS, 2)
 
         bool ok = true;
         if constexpr (C::CH) {
-            // chunk h (64 k) -> A stage h mod NA, multiplied by issuer h mod NI.
-            // Software pipeline: the next chunk is decoded while this one's TMEM
-            // store is in flight (tcgen05.wait::st comes after it).
-            uint4 cw = make_uint4(0, 0, 0, 0);
-            // codes of chunk h into cw; releases a weight stage after this set's
-            // last chunk in it (the final stage is never refilled)
-            auto load_chunk = [&](int h) -> bool {
-                const int w = h >> 3, ws = w % C::WS, uw = h & 7;
-                if (uw < 2 && !warp_wait(&wfull[ws], (w / C::WS) & 1, lane)) return false;
-                cw = *reinterpret_cast<const uint4 *>(wrow + (size_t)ws * kWStage + ((uw ^ sw) << 4));
-                if (uw >= 6 && w + 1 < nws) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&wempty[ws]);  // codes are in registers
+            // chunk h (64 k) -> A stage h mod NA, decoded by set h mod 2, multiplied
+            // by issuer h mod NI.  Software pipeline: the next chunk is decoded
+            // while this one's TMEM store is in flight (tcgen05.wait::st follows).
+            if (a.mask == nullptr) {
+                uint4 cw = make_uint4(0, 0, 0, 0);
+                // codes of chunk h into cw; releases a weight stage after this set's
+                // last chunk in it (the final stage is never refilled)
+                auto load_chunk = [&](int h) -> bool {
+                    const int w = h >> 3, ws = w % C::WS, uw = h & 7;
+                    if (uw < 2 && !warp_wait(&wfull[ws], (w / C::WS) & 1, lane)) return false;
+                    cw = *reinterpret_cast<const uint4 *>(wrow + (size_t)ws * kWStage + ((uw ^ sw) << 4));
+                    if (uw >= 6 && w + 1 < nws) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&wempty[ws]);  // codes are in registers
+                    }
+                    return true;
+                };
+                uint32_t r[32];
+                if (set < nch) {
+                    ok = load_chunk(set);
+                    decode_chunk(cw, r);
                 }
-                return true;
-            };
-            uint32_t r[32];
-            if (set < nch) {
-                ok = load_chunk(set);
-                decode_chunk(cw, r);
-            }
-            for (int h = set; h < nch && ok; h += 2) {
-                const int st = h % C::NA;
-                if (h >= C::NA && !warp_wait(&aempty[st], ((h / C::NA) - 1) & 1, lane)) {
-                    ok = false;
-                    break;
-                }
-                tc::st_32x32b_x32(tlane + (uint32_t)(st * C::ACOLS), r);
-                if (h + 2 < nch) {
-                    if (!load_chunk(h + 2)) {
+                for (int h = set; h < nch && ok; h += 2) {
+                    const int st = h % C::NA;
+                    if (h >= C::NA && !warp_wait(&aempty[st], ((h / C::NA) - 1) & 1, lane)) {
                         ok = false;
                         break;
                     }
-                    decode_chunk(cw, r);  // overlaps the store above
+                    tc::st_32x32b_x32(tlane + (uint32_t)(st * C::ACOLS), r);
+                    if (h + 2 < nch) {
+                        if (!load_chunk(h + 2)) {
+                            ok = false;
+                            break;
+                        }
+                        decode_chunk(cw, r);  // overlaps the store above
+                    }
+                    tc::wait_st();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[st]);
                 }
-                tc::wait_st();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&afull[st]);
+            } else {
+                // zero-block map: set 0 first zeroes the accumulators, then each set
+                // decodes its live chunks; an A stage's phase is its count of uses
+                if (set == 0) {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z[i] = 0u;
+                    tc::st_32x32b_x32(tlane + (uint32_t)(C::NA * C::ACOLS), z);
+                    tc::st_32x32b_x32(tlane + (uint32_t)(C::NA * C::ACOLS + 32), z);
+                    tc::wait_st();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dzero);
+                }
+                uint4 cw = make_uint4(0, 0, 0, 0);
+                // The weight-ring bookkeeping of chunk h: this set waits for a stage at
+                // its first chunk in it and releases it after its last (the final stage
+                // is never refilled); load_chunk also reads the codes into cw.
+                auto ring_wait = [&](int h) -> bool {
+                    const int w = h >> 3;
+                    return (h & 7) >= 2 || warp_wait(&wfull[w % C::WS], (w / C::WS) & 1, lane);
+                };
+                auto ring_release = [&](int h) {
+                    const int w = h >> 3;
+                    if ((h & 7) >= 6 && w + 1 < nws) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&wempty[w % C::WS]);
+                    }
+                };
+                auto load_chunk = [&](int h) -> bool {
+                    if (!ring_wait(h)) return false;
+                    const int ws = (h >> 3) % C::WS, uw = h & 7;
+                    cw = *reinterpret_cast<const uint4 *>(wrow + (size_t)ws * kWStage + ((uw ^ sw) << 4));
+                    ring_release(h);  // codes are in registers
+                    return true;
+                };
+                // this set's next live chunk at or after h (-1: a wait gave up)
+                auto next_mine = [&](int h) -> int {
+                    for (; h < nch; h += 2) {
+                        if (chunk_live(h)) return h;
+                        if (!ring_wait(h)) return -1;
+                        ring_release(h);
+                    }
+                    return nch;
+                };
+                uint32_t r[32];
+                uint32_t par = 0, used = 0;  // bit st: uses of A stage st so far mod 2, and any use
+                int h = next_mine(set);
+                if (h < 0) {
+                    ok = false;
+                } else if (h < nch) {
+                    ok = load_chunk(h);
+                    decode_chunk(cw, r);
+                }
+                while (ok && h < nch) {
+                    const int st = h % C::NA;
+                    if (((used >> st) & 1u) && !warp_wait(&aempty[st], ((par >> st) & 1u) ^ 1u, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::st_32x32b_x32(tlane + (uint32_t)(st * C::ACOLS), r);
+                    const int hn = next_mine(h + 2);
+                    if (hn < 0) {
+                        ok = false;
+                        break;
+                    }
+                    if (hn < nch) {
+                        if (!load_chunk(hn)) {
+                            ok = false;
+                            break;
+                        }
+                        decode_chunk(cw, r);  // overlaps the store above
+                    }
+                    tc::wait_st();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[st]);
+                    par ^= 1u << st;
+                    used |= 1u << st;
+                    h = hn;
+                }
             }
             if (ok && set == 0) {
-                // sum of the accumulators of the issuers that ran (issuer j's first chunk is j)
-                const int nvalid = nch < C::NI ? nch : C::NI;
-                for (int j = 0; j < nvalid && ok; ++j) {
+                // sum of the issuers' accumulators, in issuer order: without a map,
+                // of the issuers that ran (issuer j's first chunk is j); with one,
+                // of all (zeroed first), which adds the same values
+                const int nsum = (a.mask == nullptr && nch < C::NI) ? nch : C::NI;
+                for (int j = 0; j < nsum && ok; ++j) {
                     ok = warp_wait(&dfull[j], 0, lane);
                     if (!ok) break;
                     tc::fence_after_sync();

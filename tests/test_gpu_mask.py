@@ -2,7 +2,8 @@
 oracle's map bit for bit, and a masked call -- which neither loads nor
 multiplies zero blocks -- equals the unmasked call bit for bit and meets the
 oracle's tolerance, on block-sparse weights (about 30% zero blocks), on the
-decode kernel (M <= 16) and the tile kernel."""
+decode kernel, the tcgen05 skinny kernel (per-channel scales) and the tile
+kernel, including row blocks with no live block at all."""
 import numpy as np
 import pytest
 import torch
@@ -51,6 +52,8 @@ CASES = [
     (9, 300, 8192, torch.bfloat16, 0),
     (16, 3584, 3584, torch.bfloat16, 0),
     (16, 512, 1024, torch.float16, 64),
+    (24, 700, 3072, torch.bfloat16, 0),      # tcgen05 skinny kernel, 32-token tile
+    (24, 300, 2048, torch.bfloat16, 128),    # group scales: tile kernel when masked
     (33, 640, 1024, torch.bfloat16, 0),      # tile kernel from here on
     (100, 300, 2048, torch.float16, 128),
     (300, 512, 1536, torch.bfloat16, 0),
@@ -58,12 +61,16 @@ CASES = [
 
 
 def same_kernel(M, N, gs, gated=False):
-    """Whether the unmasked call runs on the kernel the masked call runs on: the
-    automatic path sends some decode shapes (M > 8, or plain layers of
-    2049..4608 rows) to the tcgen05 skinny kernel, which reads no map, while
-    masked decode shapes run on the decode kernel."""
-    if M > 16 or gs == 64:
+    """Whether the unmasked call runs on the kernel the masked call runs on.
+    Per-channel scales and 64-wide groups: always.  128- and 256-wide groups:
+    the tcgen05 skinny kernel reads no map with group scales, so masked calls
+    run on the decode kernel (M <= 16) or the tile kernel (17 <= M <= 32) where
+    the unmasked call may run on the skinny kernel (M > 8, or plain layers of
+    2049..4608 rows, at M <= 16; every M of 17..32)."""
+    if gs in (0, 64) or M > 32:
         return True
+    if M > 16:
+        return False
     if gated:
         return M <= 8
     return M <= 8 and not (2048 < N <= 4608)
@@ -89,7 +96,7 @@ def test_masked_linear_equals_unmasked(M, N, K, xdt, gs):
         check(skip, oracle_ref(x, p, s, gs), x, s, what=f"masked {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M", [2, 40])
+@pytest.mark.parametrize("M", [2, 12, 24, 40])
 def test_masked_all_zero_rows_give_zero(M):
     """Whole CTAs whose every block is zero still write their (zero) outputs."""
     N, K = 512, 2048
@@ -108,7 +115,8 @@ def test_masked_all_zero_rows_give_zero(M):
     assert torch.all(out[:, 128:448] == 0)
 
 
-@pytest.mark.parametrize("M,N,K,gs", [(1, 1000, 2048, 0), (8, 300, 4096, 128), (64, 384, 1024, 0)])
+@pytest.mark.parametrize("M,N,K,gs", [(1, 1000, 2048, 0), (8, 300, 4096, 128), (16, 700, 2048, 0),
+                                      (24, 200, 1024, 0), (64, 384, 1024, 0)])
 def test_masked_silu_mul_equals_unmasked(M, N, K, gs):
     x, p, s = sparse_inputs(M, 2 * N, K, torch.bfloat16, gs, 2)
     mask, _ = tl.block_mask(p)
