@@ -275,8 +275,10 @@ void ternary_test_set_wait_limit(int64_t cycles, int32_t stall);
 /* Testing aid: the form of the tile kernel for every later call that runs on
  * it: 0 = chosen per call by the library (default), 1 = one output tile per
  * CTA (with split K where planned), 2 = persistent CTAs (one per SM, each
- * walking a list of 128-row x 192-token tiles).  Both forms compute the same
- * sums; any other value restores 0.  Lets tests cover both forms on any shape. */
+ * walking a list of 128-row x 192-token tiles, two accumulators), 3 = persistent
+ * CTAs with 128-row x 256-token tiles and one accumulator (per-channel scales;
+ * group scales take 2).  All forms compute the same sums; any other value
+ * restores 0.  Lets tests cover every form on any shape. */
 void ternary_test_set_tile_mode(int32_t mode);
 
 #ifdef __cplusplus

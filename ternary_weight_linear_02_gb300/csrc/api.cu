@@ -29,7 +29,8 @@ std::atomic<int> g_inject_launch_failures{0};
 std::atomic<long long> g_wait_limit{0};  // 0 = the default (~0.5 s)
 std::atomic<int> g_stall{0};
 // testing aid: the tile kernel's form (ternary_test_set_tile_mode): 0 = chosen
-// per call, 1 = one tile per CTA, 2 = persistent CTAs
+// per call, 1 = one tile per CTA, 2 = persistent CTAs (192-token tiles), 3 = persistent
+// CTAs with 256-token tiles where the scales are per channel
 std::atomic<int> g_tile_mode{0};
 
 int env_int(const char *name, int dflt) {
@@ -592,7 +593,7 @@ void ternary_test_set_wait_limit(int64_t cycles, int32_t stall) {
     g_stall.store(stall ? 1 : 0);
 }
 
-void ternary_test_set_tile_mode(int32_t mode) { g_tile_mode.store(mode == 1 || mode == 2 ? mode : 0); }
+void ternary_test_set_tile_mode(int32_t mode) { g_tile_mode.store(mode >= 1 && mode <= 3 ? mode : 0); }
 
 tl_status ternary_device_status_async(int32_t *dst, int32_t clear, void *stream) {
     if (dst == nullptr) return TL_ERR_NULL;

@@ -5,12 +5,12 @@
 
 namespace tl {
 
-bool use_persist(const TileArgs &a, bool silu, int sm_count);
+int persist_form(const TileArgs &a, bool silu, bool group, int sm_count);
 
 cudaError_t launch_tile_silu(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
                              cudaStream_t st, bool pdl) {
-    if (use_persist(a, true, sm_count))
-        return launch_persist<true>(a, bf, group, out_dtype, sm_count, st, pdl);
+    const int form = persist_form(a, true, group, sm_count);
+    if (form > 0) return launch_persist<true>(a, bf, group, out_dtype, sm_count, st, pdl, form);
     return launch_tile_any<true>(a, bf, group, out_dtype, 0, st, pdl);  // no split K
 }
 

@@ -163,7 +163,8 @@ struct TileArgs {
     int mask_words;          // map words per 128-row block
     int sk;                  // K split = cluster size along grid z (set by the launcher)
     int cpc;                 // 64-k chunks per CTA of the split (set by the launcher)
-    int persist;             // -1: the launcher decides; 0: one tile per CTA; 1: persistent CTAs
+    int persist;             // -1: the launcher decides; 0: one tile per CTA; 1: persistent CTAs,
+                             // 192-token tiles; 2: persistent, 256-token tiles (per-channel scales)
 };
 
 bool tile_supported(int64_t M, int64_t N, int64_t K);  // K % 64 == 0

@@ -1,7 +1,11 @@
 // tile_persist.cuh -- the persistent variant of the tile kernel (tile.cuh) for
-// many output tiles: one CTA per SM walks a list of 128-row x 192-token tiles,
-// so set-up, pipeline fill and the epilogue of one tile overlap the main loop
-// of the next.
+// many output tiles: one CTA per SM walks a list of 128-row x PBN-token tiles,
+// so set-up and pipeline fill are paid once.  PBN = 192: two TMEM accumulators,
+// the epilogue of one tile overlapping the main loop of the next.  PBN = 256
+// (per-channel scales): one accumulator and four A stages; the issuer waits for
+// the epilogue to read the accumulator out, but each MMA instruction carries a
+// third more work -- one warp issues tcgen05.mma at a fixed rate whatever N is,
+// and that rate bounds the 192-token form.
 //
 // Same arithmetic as the tile kernel (ternary codes of "三元量化模型接入vLLM：
 // 从逆向加载到Kernel优化的完整实战" §3.1 decoded to 2t in 16-bit registers,
@@ -13,13 +17,13 @@
 //    chunk's 16 code bytes four items ahead and storing the decoded chunk into
 //    a TMEM A stage (a stage holds two chunks of one tile: one round of barrier
 //    waits and commits per stage);
-//  * warp 8, producer: TMA of x tiles (192 tokens x 64 k per chunk) into a ring
+//  * warp 8, producer: TMA of x tiles (PBN tokens x 64 k per chunk) into a ring
 //    of stages that also runs across tiles;
 //  * warp 9: TMEM allocation and the MMA issuer; tile i accumulates into TMEM
-//    buffer i % 2 (two 192-column accumulators + the A stages = 512 columns);
-//  * warps 4-7, epilogue: read buffer i % 2 with tcgen05.ld, hand it back to
+//    buffer i % NB (NB accumulators of PBN columns + the A stages = 512 columns);
+//  * warps 4-7, epilogue: read buffer i % NB with tcgen05.ld, hand it back to
 //    the issuer as soon as the last columns are in registers, scale, convert
-//    and store -- while the issuer already fills the other buffer.  The gated
+//    and store -- with two buffers, while the issuer already fills the other.  The gated
 //    variant (64 gate + 64 up rows per tile) exchanges rows through a 16 KB
 //    shared-memory buffer, 32 tokens at a time.
 // Tiles are numbered with the token tile fastest, so the CTAs running at the
@@ -36,25 +40,26 @@ namespace tl {
 
 namespace {
 
-constexpr int kPBN = 192;                     // tokens per tile
 constexpr int kPWarps = 10;
 constexpr int kPThreads = 32 * kPWarps;
 constexpr int kPWarpEpi0 = 4, kPWarpProd = 8, kPWarpMma = 9;
 
-template <int SMODE>
+template <int SMODE, int PBN>
 struct PCfg {
     // A pipeline stage holds up to CPS consecutive live chunks of one tile (one
     // round of waits and commits per stage: the rounds, not the MMA rate, bound
-    // the loop at one chunk per round); two A stages + two accumulators fill the
-    // 512 TMEM columns.
+    // the loop at one chunk per round); the A stages and the NB accumulators
+    // fill the 512 TMEM columns.
+    static_assert(PBN == 192 || (PBN == 256 && SMODE == kChannel), "tile widths");
+    static constexpr int NB = PBN == 256 ? 1 : 2;             // accumulators
     static constexpr int CPS = (SMODE == kSplit) ? 1 : 2;
     static constexpr int ACOLS = (SMODE == kSplit) ? 64 : 32;  // TMEM columns per chunk of A
-    static constexpr int NA = 128 / (ACOLS * CPS);             // A stages
+    static constexpr int NA = (512 - NB * PBN) / (ACOLS * CPS);  // A stages
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int DCOL0 = NA * CPS * ACOLS;             // accumulators at DCOL0 + {0, kPBN}
-    static_assert(DCOL0 + 2 * kPBN <= 512, "tensor memory budget");
+    static constexpr int DCOL0 = NA * CPS * ACOLS;             // accumulators at DCOL0 + b * PBN
+    static_assert(NA >= 2 && DCOL0 + NB * PBN <= 512, "tensor memory budget");
     static constexpr int NS = (CPS == 2) ? 3 : 4;              // x stages
-    static constexpr int XCHUNK = kPBN * 128;                  // x of one chunk: 192 rows x 128 B
+    static constexpr int XCHUNK = PBN * 128;                   // x of one chunk: PBN rows x 128 B
     static constexpr int XSTAGE = CPS * XCHUNK;
     static constexpr int EX_OFF = NS * XSTAGE;                 // gated exchange [32 tokens][128 rows]
     static constexpr int EX_BYTES = 32 * 128 * 4;
@@ -69,10 +74,10 @@ struct PCfg {
     static_assert(SMEM_REQ + 1024 <= 228 * 1024, "shared memory");
 };
 
-template <bool BF, int SMODE, int OUT, bool SILU>
+template <bool BF, int SMODE, int OUT, bool SILU, int PBN>
 __global__ void __launch_bounds__(kPThreads, 1)
     tile_persist_kernel(const __grid_constant__ CUtensorMap tmx, TileArgs a) {
-    using C = PCfg<SMODE>;
+    using C = PCfg<SMODE, PBN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -87,7 +92,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nchunks = a.K / kKC;
     const int RB = SILU ? (a.nh + 63) / 64 : (a.N + 127) / 128;  // row blocks
-    const int MB = (a.M + kPBN - 1) / kPBN;                       // token tiles
+    const int MB = (a.M + PBN - 1) / PBN;                         // token tiles
     const int T = RB * MB;
 
     if (threadIdx.x == 0) {
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (a.status) atomicExch(a.status, kStatusTimeout);
     };
     // tile t: token tile t % MB (fastest), row block t / MB
-    auto tile_m0 = [&](int t) { return (t % MB) * kPBN; };
+    auto tile_m0 = [&](int t) { return (t % MB) * PBN; };
     auto tile_rb = [&](int t) { return t / MB; };
     // weight row of TMEM lane r in tile t, and whether it exists
     auto row_of = [&](int t, int r, bool &ok) -> int {
@@ -192,19 +197,19 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
         }
     } else if (warp == kPWarpMma) {
-        // ---------------- MMA issuer: tile i into accumulator i % 2
+        // ---------------- MMA issuer: tile i into accumulator i % NB
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_f16(kPBN, BF);
+            constexpr uint32_t idesc = tc::idesc_f16(PBN, BF);
             int st = 0, i = 0;
             bool ok = true;
             for (int t = blockIdx.x; ok && t < T; t += gridDim.x, ++i) {
-                const int buf = i & 1;
-                if (i >= 2 && !mbar_wait_bounded(&dempty[buf], ((i >> 1) - 1) & 1)) {
+                const int buf = i % C::NB;
+                if (i >= C::NB && !mbar_wait_bounded(&dempty[buf], ((i / C::NB) - 1) & 1)) {
                     give_up();
                     break;
                 }
                 tc::fence_after_sync();
-                const uint32_t dcol = tmem + (uint32_t)(C::DCOL0 + buf * kPBN);
+                const uint32_t dcol = tmem + (uint32_t)(C::DCOL0 + buf * PBN);
                 int tlc = 0;  // live chunks of this tile
                 for (int c = next_live(t, 0); c < nchunks; ++st) {
                     const int s = st % C::NA, xs = st % C::NS;
@@ -368,8 +373,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float *ex = reinterpret_cast<float *>(smem + C::EX_OFF);  // [32 tokens][128 rows]
         int i = 0;
         for (int t = blockIdx.x; t < T; t += gridDim.x, ++i) {
-            const int buf = i & 1;
-            bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&dfull[buf], (i >> 1) & 1));
+            const int buf = i % C::NB;
+            bool got = __all_sync(0xffffffffu, mbar_wait_bounded(&dfull[buf], (i / C::NB) & 1));
             if (!got) give_up();
             got = got && !*abort_flag;
             if constexpr (SILU) {
@@ -388,13 +393,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const bool empty = next_live(t, 0) >= nchunks;  // no live chunk: D never written
             float sc = 1.f;  // channel mode: A held 2*t, so D = 2*sum(t x); group modes: A held t*s
             if constexpr (SMODE == kChannel) sc = 0.5f * (rowok ? h2f(a.scale[n]) : 0.f);
-            const uint32_t dbase = tmem + (uint32_t)(C::DCOL0 + buf * kPBN) + ((uint32_t)(e * 32) << 16);
+            const uint32_t dbase = tmem + (uint32_t)(C::DCOL0 + buf * PBN) + ((uint32_t)(e * 32) << 16);
 #pragma unroll 1
-            for (int j = 0; j < kPBN / 32; ++j) {
+            for (int j = 0; j < PBN / 32; ++j) {
                 uint32_t d[32];
                 tc::ld_32x32b_x32(dbase + (uint32_t)(j * 32), d);
                 tc::wait_ld();
-                if (j == kPBN / 32 - 1) {  // every column is in registers: the issuer may reuse the buffer
+                if (j == PBN / 32 - 1) {  // every column is in registers: the issuer may reuse the buffer
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&dempty[buf]);
@@ -442,36 +447,42 @@ __global__ void __launch_bounds__(kPThreads, 1)
 constexpr double kP192 = 0.87;
 
 // Cost, in 64-k chunk times of a 256-token tile, of running `a` on the persistent
-// kernel: the busiest CTA's tiles x (chunks + a small per-tile part), plus one
-// CTA's fixed set-up.
-inline double persist_cost(const TileArgs &a, bool silu, int sm_count) {
+// kernel with PBN-token tiles: the busiest CTA's tiles x (chunks + a per-tile
+// part), plus one CTA's fixed set-up.  With one accumulator (PBN = 256) the
+// per-tile part holds the epilogue's read-out, which the issuer waits for: ~4
+// chunk times for a plain output, ~25 for the gated one, whose 32-token
+// exchange rounds all sit on that path (fitted to the 7B shapes at M = 1024 and
+// 2048: q/k/v 28.0 / 51.9 us against 31.3 / 60.3 one tile per CTA; gate/up
+// 568 us against 478 with 192-token tiles).
+inline double persist_cost(const TileArgs &a, bool silu, int sm_count, int pbn = 192) {
     const int64_t rb = silu ? (a.nh + 63) / 64 : (a.N + 127) / 128;
-    const int64_t tiles = rb * ((a.M + kPBN - 1) / kPBN);
+    const int64_t tiles = rb * ((a.M + pbn - 1) / pbn);
     const int64_t ctas = tiles < sm_count ? tiles : sm_count;
     const int64_t per_cta = (tiles + ctas - 1) / ctas;
+    if (pbn == 256) return (double)per_cta * (a.K / kKC + (silu ? 25.0 : 4.0)) + 12.0;
     return (double)per_cta * (a.K / kKC + 2.0) * kP192 + 18.0;
 }
 
-template <bool BF, int SMODE, int OUT, bool SILU>
+template <bool BF, int SMODE, int OUT, bool SILU, int PBN>
 cudaError_t launch_persist_one(const TileArgs &a, int sm_count, cudaStream_t st, bool pdl) {
-    using C = PCfg<SMODE>;
+    using C = PCfg<SMODE, PBN>;
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap map;
     const cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.M};
     const cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)kPBN};
+    const cuuint32_t box[2] = {(cuuint32_t)kKC, (cuuint32_t)PBN};
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(&map, BF ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                      const_cast<uint16_t *>(a.x), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-    auto kern = tile_persist_kernel<BF, SMODE, OUT, SILU>;
+    auto kern = tile_persist_kernel<BF, SMODE, OUT, SILU, PBN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_REQ);
     if (e != cudaSuccess) return e;
     const int64_t rb = SILU ? (a.nh + 63) / 64 : (a.N + 127) / 128;
-    const int64_t tiles = rb * ((a.M + kPBN - 1) / kPBN);
+    const int64_t tiles = rb * ((a.M + PBN - 1) / PBN);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(tiles < sm_count ? tiles : sm_count), 1, 1);
     cfg.blockDim = dim3(kPThreads, 1, 1);
@@ -488,16 +499,26 @@ cudaError_t launch_persist_one(const TileArgs &a, int sm_count, cudaStream_t st,
     return cudaLaunchKernelEx(&cfg, kern, map, b);
 }
 
+// pbn: 192 or 256 (256 with per-channel scales only; group scales take 192)
 template <bool SILU>
 cudaError_t launch_persist(const TileArgs &a, bool bf, bool group, int out_dtype, int sm_count,
-                           cudaStream_t st, bool pdl) {
+                           cudaStream_t st, bool pdl, int pbn = 192) {
     auto go = [&](auto bfc, auto smc) -> cudaError_t {
         constexpr bool B = decltype(bfc)::value;
         constexpr int S = decltype(smc)::value;
+        if constexpr (S == kChannel) {
+            if (pbn == 256) {
+                switch (out_dtype) {
+                case 0: return launch_persist_one<B, S, 0, SILU, 256>(a, sm_count, st, pdl);
+                case 1: return launch_persist_one<B, S, 1, SILU, 256>(a, sm_count, st, pdl);
+                default: return launch_persist_one<B, S, 2, SILU, 256>(a, sm_count, st, pdl);
+                }
+            }
+        }
         switch (out_dtype) {
-        case 0: return launch_persist_one<B, S, 0, SILU>(a, sm_count, st, pdl);
-        case 1: return launch_persist_one<B, S, 1, SILU>(a, sm_count, st, pdl);
-        default: return launch_persist_one<B, S, 2, SILU>(a, sm_count, st, pdl);
+        case 0: return launch_persist_one<B, S, 0, SILU, 192>(a, sm_count, st, pdl);
+        case 1: return launch_persist_one<B, S, 1, SILU, 192>(a, sm_count, st, pdl);
+        default: return launch_persist_one<B, S, 2, SILU, 192>(a, sm_count, st, pdl);
         }
     };
     using T_ = std::true_type;

@@ -1,9 +1,11 @@
 """The persistent form of the tile kernel against the oracle.
 
-One CTA per SM walks a list of 128-row x 192-token tiles with two TMEM
-accumulators, the epilogue of one tile overlapping the main loop of the next.
-ternary_test_set_tile_mode(2) makes every tile-kernel call in this module use
-it, whatever its shape, so the cases cover: one tile and many tiles per CTA,
+One CTA per SM walks a list of tiles: 128 rows x 192 tokens with two TMEM
+accumulators, the epilogue of one tile overlapping the main loop of the next
+(tile mode 2), or 128 rows x 256 tokens with one accumulator (tile mode 3,
+per-channel scales; group scales fall back to 192).  The module runs once per
+mode; ternary_test_set_tile_mode makes every tile-kernel call use that form,
+whatever its shape, so the cases cover: one tile and many tiles per CTA,
 ragged M (partial last token tile) and N (partial last row block), every scale
 mode (per channel; fp16 x with folded group scales; bf16 x with split group
 scales; 32- to 256-wide groups), every output dtype, the SiLU-gated variant
@@ -26,15 +28,15 @@ DEV = "cuda"
 F16, BF16, F32 = torch.float16, torch.bfloat16, torch.float32
 
 
-@pytest.fixture(scope="module", autouse=True)
-def _persistent():
+@pytest.fixture(scope="module", autouse=True, params=[2, 3], ids=["tiles192", "tiles256"])
+def _persistent(request):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     tl.build()
     oracle.build()
     lib = tl.load()
-    lib.ternary_test_set_tile_mode(2)
-    yield
+    lib.ternary_test_set_tile_mode(request.param)
+    yield request.param
     lib.ternary_test_set_tile_mode(0)
 
 
@@ -52,7 +54,9 @@ CASES = [
     # M, N, K, x dtype, group size, out dtype
     (33, 128, 1024, BF16, 0, F32),        # one tile
     (192, 300, 2048, F16, 0, F32),        # exactly one token tile, ragged N
-    (193, 129, 4096, BF16, 0, BF16),      # a second token tile holding one token
+    (193, 129, 4096, BF16, 0, BF16),      # a second 192-token tile holding one token
+    (256, 300, 2048, BF16, 0, F32),       # exactly one 256-token tile
+    (257, 129, 2048, F16, 0, BF16),       # a second 256-token tile holding one token
     (400, 1000, 1024, BF16, 128, F32),    # bf16 x, split group scales
     (400, 1000, 1024, F16, 128, F16),     # fp16 x, folded group scales
     (300, 513, 2048, BF16, 32, F32),      # 32-wide groups
@@ -118,7 +122,7 @@ def test_persist_every_byte_exact():
     assert np.array_equal(y.cpu().double().numpy(), want)
 
 
-def test_persist_repeatable_and_one_tile_per_cta_form():
+def test_persist_repeatable_and_one_tile_per_cta_form(_persistent):
     """Bit-identical across calls; the one-tile-per-CTA form (here with split K)
     meets the same bound against the oracle."""
     lib = tl.load()
@@ -130,7 +134,7 @@ def test_persist_repeatable_and_one_tile_per_cta_form():
         c = tl.linear(x, p, s, 0, out_dtype=F32, path="tile")
         torch.cuda.synchronize()
     finally:
-        lib.ternary_test_set_tile_mode(2)
+        lib.ternary_test_set_tile_mode(_persistent)
     assert torch.equal(a, b)
     want = oracle_ref(x, p, s, 0)
     check(a, want, x, s, what="persistent")
